@@ -1,0 +1,484 @@
+"""Benchmark of the block-scaled quantization + GEMM hot path on GB300.
+
+One step = one pass over every row of the hot path, each on its own seeded synthetic workload
+(all inputs resident in HBM before the timed region):
+  q2   MXFP8 quantize of 16384x4096 bf16 activations (4 outlier channels), E4M3 and E5M2,
+       row-wise + column-wise in one pass each
+  lin  MXFP8 linear layer M=8192 K=4096 N=14336: quantize X, W (E4M3) and G (E5M2) row- and
+       column-wise, then fprop Y = X W^T, dgrad dX = G W, wgrad dW = G^T X (bf16 out)
+  nv   NVFP4 8192^3: two-pass quantize of A and B, block-scaled FP4 GEMM (FP32 out)
+  ds   DeepSeek FP8 M=4096 K=7168 N=2048: 1x128 / 128x128 quantize, GEMM with FP32 promotion
+       every 128 of K (bf16 out)
+value = sum of GEMM FLOPs in the step / step time (TFLOP/s); per-row times, GB/s, TFLOP/s and
+roofline fractions are reported under "rows".  Every input exceeds or, within one step, is
+separated from its next use by far more than the 129 MB L2, so no explicit flush is needed.
+
+--impl reference times the CPU oracle (the plain C reference) on a bounded sample of the same
+step and prints the same metric.  Multi-GPU runs (torchrun) are independent replicas: the path
+has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MXFP8 GEMM TFLOP/s & quantize GB/s on 1 GB300 (fraction of roofline)"
+WORKLOAD = "mxfp8_q16384x4096+mxfp8_linear_8192x4096x14336+nvfp4_8192^3+deepseek_fp8_4096x7168x2048"
+
+# algorithmic work per call
+F_LIN = 2 * 8192 * 4096 * 14336            # each of fprop / dgrad / wgrad
+F_NV = 2 * 8192 ** 3
+F_DS = 2 * 4096 * 7168 * 2048
+GEMM_FLOPS_STEP = 3 * F_LIN + F_NV + F_DS
+
+
+def mx_q_bytes(rows, cols, both=True):
+    # read bf16 + write codes (1 B) + E8M0 scales (1/32 B) for each copy
+    return rows * cols * (2 + (2 if both else 1) * (1 + 1 / 32))
+
+
+def nv_q_bytes(rows, cols):
+    # two reads of bf16 (amax pass, quantize pass) + packed codes (1/2 B) + UE4M3 scales (1/16 B)
+    return rows * cols * (2 + 2 + 0.5 + 1 / 16)
+
+
+def ds_q_bytes(rows, cols, tile_rows):
+    return rows * cols * (2 + 1) + 4 * (rows // tile_rows) * (cols // 128)
+
+
+Q2_BYTES = 2 * mx_q_bytes(16384, 4096)
+LINQ_BYTES = mx_q_bytes(8192, 4096) + mx_q_bytes(14336, 4096) + mx_q_bytes(8192, 14336)
+NVQ_BYTES = 2 * nv_q_bytes(8192, 8192)
+DSQ_BYTES = ds_q_bytes(4096, 7168, 1) + ds_q_bytes(2048, 7168, 128)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1] or [s for (_, s) in self.samples]
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------------------------ workload
+class Workload:
+    """All inputs and outputs of one step, resident on the device."""
+
+    def __init__(self, dev):
+        import torch
+        from block_scaled_precision_mx_gb300 import synthetic
+        import block_scaled_precision_mx_gb300 as mx
+        self.mx = mx
+        self.torch = torch
+        self.dev = dev
+        t = lambda x: x.to(dev)
+        self.host = {}
+        self.host["x2"] = synthetic.mxfp8_quantize()
+        self.host["X"], self.host["W"], self.host["G"] = synthetic.mxfp8_linear()
+        self.host["A4"], self.host["B4"] = synthetic.nvfp4_pair()
+        self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
+        self.d = {k: t(v) for k, v in self.host.items()}
+        u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
+        f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)
+        bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
+        sb = mx.mx_scale_bytes
+        # q2 outputs (E4M3 and E5M2)
+        self.q2 = {e: (u8(16384, 4096), u8(sb(16384, 4096)), u8(4096, 16384), u8(sb(4096, 16384))) for e in (0, 1)}
+        self.Xq = (u8(8192, 4096), u8(sb(8192, 4096)), u8(4096, 8192), u8(sb(4096, 8192)))
+        self.Wq = (u8(14336, 4096), u8(sb(14336, 4096)), u8(4096, 14336), u8(sb(4096, 14336)))
+        self.Gq = (u8(8192, 14336), u8(sb(8192, 14336)), u8(14336, 8192), u8(sb(14336, 8192)))
+        self.Y, self.dX, self.dW = bf(8192, 14336), bf(8192, 4096), bf(14336, 4096)
+        self.A4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
+        self.B4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
+        self.Y4 = f32(8192, 8192)
+        self.A5q = (u8(4096, 7168), f32(56, 4096))
+        self.B5q = (u8(2048, 7168), f32(16, 56))
+        self.Y5 = bf(4096, 2048)
+        self.launches_per_step = 2 + 6 + 5 + 3
+
+    def outputs(self):
+        return [self.q2[0][0], self.q2[0][2], self.q2[1][0], self.q2[1][2], self.Y, self.dX, self.dW, self.Y4, self.Y5]
+
+    def step(self, ev=None):
+        """One pass of the hot path.  `ev(name)` records a CUDA event at row boundaries."""
+        mx = self.mx
+        d = self.d
+        mark = ev or (lambda name: None)
+        mark("q2")
+        for e in (0, 1):
+            q = self.q2[e]
+            mx.mx_quantize(d["x2"], elem=e, layout=mx.BOTH, q_row=q[0], s_row=q[1], q_col=q[2], s_col=q[3])
+        mark("linq")
+        for src, dst, e in ((d["X"], self.Xq, 0), (d["W"], self.Wq, 0), (d["G"], self.Gq, 1)):
+            mx.mx_quantize(src, elem=e, layout=mx.BOTH, q_row=dst[0], s_row=dst[1], q_col=dst[2], s_col=dst[3])
+        mark("fprop")
+        mx.mx_gemm(self.Xq[0], self.Xq[1], 0, self.Wq[0], self.Wq[1], 0, 8192, 14336, 4096, mx.OUT_BF16, out=self.Y)
+        mark("dgrad")
+        mx.mx_gemm(self.Gq[0], self.Gq[1], 1, self.Wq[2], self.Wq[3], 0, 8192, 4096, 14336, mx.OUT_BF16, out=self.dX)
+        mark("wgrad")
+        mx.mx_gemm(self.Gq[2], self.Gq[3], 1, self.Xq[2], self.Xq[3], 0, 14336, 4096, 8192, mx.OUT_BF16, out=self.dW)
+        mark("nvq")
+        for src, dst in ((d["A4"], self.A4q), (d["B4"], self.B4q)):
+            mx.nvfp4_quantize(src, q_packed=dst[0], s_ue4m3=dst[1], gscale=dst[2], workspace=dst[3])
+        mark("nvgemm")
+        mx.nvfp4_gemm(self.A4q[0], self.A4q[1], self.A4q[2], self.B4q[0], self.B4q[1], self.B4q[2], 8192, 8192,
+                      8192, mx.OUT_F32, out=self.Y4)
+        mark("dsq")
+        mx.mx_quantize(d["A5"], block=128, block_rows=1, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                       q_row=self.A5q[0], s_row=self.A5q[1])
+        mx.mx_quantize(d["B5"], block=128, block_rows=128, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                       q_row=self.B5q[0], s_row=self.B5q[1])
+        mark("dsgemm")
+        mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
+                              out=self.Y5)
+        mark("end")
+
+
+ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm"]
+
+
+def row_report(name, ms, peaks):
+    """Per-row throughput and roofline fraction from its average time per step (ms)."""
+    s = ms / 1e3
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (nominal ratio)
+    fp4_peak = 4.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 4x BF16 (nominal ratio)
+    if name in ("q2", "linq", "nvq", "dsq"):
+        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES}[name]
+        gbs = b / s / 1e9
+        return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "bound": "hbm", "bytes": int(b)}
+    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS}[name]
+    tf = f / s / 1e12
+    peak = fp4_peak if name == "nvgemm" else fp8_peak
+    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
+            "flops": int(f)}
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+def oracle_sample_run():
+    """Time the CPU oracle on a bounded sample of one step; returns (projected step seconds,
+    description, threads)."""
+    import numpy as np
+    import oracle as orc
+    from block_scaled_precision_mx_gb300 import synthetic
+    orc.build()
+    t_total = 0.0
+    parts = []
+
+    def timed(fn, scale, what):
+        nonlocal t_total
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        t_total += dt * scale
+        parts.append(f"{what} x{scale:g}")
+
+    x2 = synthetic.mxfp8_quantize(rows=256, cols=4096)
+    timed(lambda: [(orc.mx_quantize_rowwise(x2, f), orc.mx_quantize_colwise(x2, f)) for f in (0, 1)], 16384 / 256,
+          "q2 256 rows")
+    X, W, G = synthetic.mxfp8_linear(M=256, K=4096, N=256)
+    Gw = synthetic.normal(256, 14336, 1e-3, 3002)
+    def linq():
+        for src, f in ((X, 0), (W, 0)):
+            orc.mx_quantize_rowwise(src, f)
+            orc.mx_quantize_colwise(src, f)
+    timed(linq, (8192 + 14336) / 512, "X,W quantize 256 rows")
+    timed(lambda: (orc.mx_quantize_rowwise(Gw, 1), orc.mx_quantize_colwise(Gw, 1)), 8192 / 256, "G quantize 256 rows")
+    # GEMMs: a few output rows of each at full N and K
+    rng = np.random.default_rng(0)
+    def gemm_rows(M, N, K, fa, fb, rows):
+        qa = rng.integers(0, 0x7E, (rows, K), dtype=np.uint8)
+        qb = rng.integers(0, 0x7E, (N, K), dtype=np.uint8)
+        sa = np.full((rows, K // 32), 127, np.uint8)
+        sb = np.full((N, K // 32), 127, np.uint8)
+        timed(lambda: orc.mx_gemm(qa, sa, fa, qb, sb, fb), M / rows, f"mx gemm {rows} rows of {M}x{N}x{K}")
+    gemm_rows(8192, 14336, 4096, 0, 0, 4)
+    gemm_rows(8192, 4096, 14336, 1, 0, 4)
+    gemm_rows(14336, 4096, 8192, 1, 0, 4)
+    a4 = synthetic.with_sparse_outliers(128, 8192, 4000)
+    timed(lambda: orc.nv_quantize(a4), 2 * 8192 / 128, "nvfp4 quantize 128 rows")
+    qa4 = rng.integers(0, 256, (2, 4096), dtype=np.uint8)
+    qb4 = rng.integers(0, 256, (8192, 4096), dtype=np.uint8)
+    s4a = np.full((2, 512), 0x38, np.uint8)
+    s4b = np.full((8192, 512), 0x38, np.uint8)
+    timed(lambda: orc.nv_gemm(qa4, s4a, 1.0, qb4, s4b, 1.0), 8192 / 2, "nvfp4 gemm 2 rows of 8192^3")
+    a5 = synthetic.normal(256, 7168, 1.0, 5000)
+    timed(lambda: orc.ds_quantize_1x128(a5), 4096 / 256, "ds 1x128 quantize 256 rows")
+    b5 = synthetic.normal(256, 7168, 0.02, 5001)
+    timed(lambda: orc.ds_quantize_128x128(b5), 2048 / 256, "ds 128x128 quantize 256 rows")
+    qa5 = rng.integers(0, 0x7E, (4, 7168), dtype=np.uint8)
+    qb5 = rng.integers(0, 0x7E, (2048, 7168), dtype=np.uint8)
+    timed(lambda: orc.ds_gemm(qa5, np.ones((4, 56), np.float32), qb5, np.ones((16, 56), np.float32)), 4096 / 4,
+          "ds gemm 4 rows of 4096x2048x7168")
+    return t_total, "; ".join(parts), orc.num_threads()
+
+
+# ------------------------------------------------------------------------------------ main
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    t_steps = []
+    desc = threads = None
+    for i in range(args.warmup + args.steps):
+        t, desc, threads = oracle_sample_run()
+        if i >= args.warmup:
+            t_steps.append(t)
+    t_step = statistics.median(t_steps)
+    value = GEMM_FLOPS_STEP / t_step / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample": "bounded sample of each row, projected to the full step"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_env()
+    # the oracle's OpenMP pool is created before the first GPU call
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample_run()
+
+    import torch
+    import block_scaled_precision_mx_gb300 as mx
+    from block_scaled_precision_mx_gb300 import build as mxbuild
+    mxbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    peaks = load_peaks()
+
+    wl = Workload(dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        wl.step()
+    assert mx.mx_check() == mx.MX_OK
+
+    # per-row events over the timed steps
+    evs = []
+
+    def mark_factory(lst):
+        def mark(name):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            lst.append((name, e))
+        return mark
+
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if os.environ.get(
+        "CUDA_VISIBLE_DEVICES") else str(local)
+    sampler = ClockSampler(phys)
+    sampler.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        lst = []
+        wl.step(mark_factory(lst))
+        evs.append(lst)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if pg:
+        pg.barrier()
+    sampler.stop()
+    status = mx.mx_check()
+    if status != mx.MX_OK:
+        raise RuntimeError(f"device status after timed region: {mx.status_string(status)}")
+    ms_total = start.elapsed_time(stop)
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    rows_ms = {n: 0.0 for n in ROW_ORDER}
+    for lst in evs:
+        for (n, e0), (_, e1) in zip(lst[:-1], lst[1:]):
+            rows_ms[n] += e0.elapsed_time(e1)
+    rows_ms = {n: v / args.steps for n, v in rows_ms.items()}
+    rows = {n: row_report(n, rows_ms[n], peaks) for n in ROW_ORDER}
+
+    # dominant kernel: the largest share of the step
+    dom = max(ROW_ORDER, key=lambda n: rows_ms[n])
+    launches_in_row = {"q2": 2, "linq": 3, "fprop": 1, "dgrad": 1, "wgrad": 1, "nvq": 4, "nvgemm": 1, "dsq": 2,
+                       "dsgemm": 1}
+    rep = rows[dom]
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(dom)
+    if rep["bound"] == "tensor":
+        roof = {"bound": "tensor", "kernel": dom, "achieved": rep["TFLOP/s"], "unit": "TFLOP/s",
+                "peak": round(rep["TFLOP/s"] / rep["frac"], 1) if rep["frac"] else None,
+                "frac": rep["frac"], "traffic": traffic,
+                "peak_source": f"{peaks['source']}: bf16 sustained x {'4 (FP4)' if dom == 'nvgemm' else '2 (FP8)'}"
+                               " nominal dense ratio"}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": rep["GB/s"], "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                "frac": rep["frac"], "traffic": traffic, "peak_source": f"{peaks['source']} copy bandwidth"}
+    roof["launches_per_step"] = launches_in_row[dom]
+
+    # end to end through the public API with host buffers
+    e2e = None
+    h2d = sum(v.numel() * v.element_size() for v in wl.host.values())
+    outs = wl.outputs()
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    if args.e2e_steps > 0:
+        pinned_in = {k: v.pin_memory() for k, v in wl.host.items()}
+        pinned_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+        def e2e_step():
+            for k, v in pinned_in.items():
+                wl.d[k].copy_(v, non_blocking=True)
+            wl.step()
+            for o, p in zip(outs, pinned_out):
+                p.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if pg:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * GEMM_FLOPS_STEP / (e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    value = world * GEMM_FLOPS_STEP / (ms_step / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8/fp4 inputs, f32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (129 MB) between reuses; no explicit flush",
+                   "quantize_GB/s": round((Q2_BYTES + LINQ_BYTES + NVQ_BYTES + DSQ_BYTES) /
+                                          (sum(rows_ms[n] for n in ('q2', 'linq', 'nvq', 'dsq')) / 1e3) / 1e9, 1)},
+        "rows": rows,
+        "roofline": roof,
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if cpu is not None:
+        t_cpu, desc, threads = cpu
+        line["cpu_baseline"] = {"value": round(GEMM_FLOPS_STEP / t_cpu / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": threads, "kind": "oracle", "sample": desc,
+                                "projected_step_s": round(t_cpu, 2)}
+    if rank == 0:
+        print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

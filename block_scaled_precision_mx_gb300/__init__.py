@@ -1,0 +1,224 @@
+"""GB300 (sm_103a) block-scaled quantization and GEMMs: MXFP8, NVFP4, DeepSeek FP8.
+
+Thin Python binding over the C ABI of ``libmxgb.so`` (declared in include/mx.h).
+Every function here only marshals arguments: tensors are torch CUDA tensors
+(device memory), the stream is torch's current stream unless one is given,
+and every step of the computation runs in the library's CUDA kernels.  There
+is no CPU fallback: if the library cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI):
+  mx_quantize, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
+  mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+# enums (include/mx.h)
+MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(5)
+E4M3, E5M2, E2M1 = 0, 1, 2
+SCALE_E8M0, SCALE_UE4M3, SCALE_FP32 = 0, 1, 2
+ROWWISE, COLWISE, BOTH = 1, 2, 3
+OUT_F32, OUT_BF16 = 0, 1
+
+EXPORTS = (
+    "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
+    "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
+)
+
+
+class MxError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libmxgb.so (built by build.py / __graft_entry__.build()).  Raises if missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmxgb.so not built ({_LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        fp = ctypes.POINTER(ctypes.c_float)
+        sig = {
+            "mx_abi_version": (i32, []),
+            "mx_status_string": (ctypes.c_char_p, [i32]),
+            "mx_quantize": (i32, [vp, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]),
+            "mx_gemm": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, vp, i32, i64, vp]),
+            "nvfp4_workspace_bytes": (ctypes.c_size_t, [i64, i64]),
+            "nvfp4_quantize": (i32, [vp, i64, i64, vp, vp, vp, vp, vp]),
+            "nvfp4_gemm": (i32, [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, i32, i64, vp]),
+            "fp8_blockwise_gemm": (i32, [vp, vp, vp, vp, i64, i64, i64, vp, i32, i64, vp]),
+            "mx_scale_bytes": (ctypes.c_size_t, [i64, i64, i32, i32, i32]),
+            "mx_check": (i32, [vp]),
+            "mx_num_sms": (i32, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().mx_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != MX_OK:
+        raise MxError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensor arguments must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _u8(n, device):
+    return torch.empty(int(n), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ sizes
+def mx_scale_bytes(rows: int, cols: int, block: int = 32, block_rows: int = 1, sfmt: int = SCALE_E8M0) -> int:
+    return int(load().mx_scale_bytes(rows, cols, block, block_rows, sfmt))
+
+
+def nvfp4_workspace_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_workspace_bytes(rows, cols))
+
+
+# ------------------------------------------------------------------ quantizers
+def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int = E4M3,
+                sfmt: int = SCALE_E8M0, layout: int = BOTH, q_row=None, s_row=None, q_col=None,
+                s_col=None, stream=None):
+    """Block-quantize bf16 x[rows][cols] (see include/mx.h, mx_quantize).
+
+    Returns (q_row, s_row, q_col, s_col); outputs not given are allocated (torch), copies not
+    requested are None.  MX scales are returned as flat uint8 tensors in the GEMM layout;
+    DeepSeek FP32 scales as float tensors ([cols/128][rows] for 1x128, [rows/128][cols/128]
+    for 128x128)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    row, col = bool(layout & ROWWISE), bool(layout & COLWISE)
+    if sfmt == SCALE_FP32:
+        if row and q_row is None:
+            q_row = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+        if row and s_row is None:
+            shape = (cols // 128, rows) if block_rows == 1 else (rows // 128, cols // 128)
+            s_row = torch.empty(shape, dtype=torch.float32, device=dev)
+    else:
+        nb = mx_scale_bytes(rows, cols, block, block_rows, sfmt)
+        if row and q_row is None:
+            q_row = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+        if row and s_row is None:
+            s_row = _u8(nb, dev)
+        if col and q_col is None:
+            q_col = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
+        if col and s_col is None:
+            s_col = _u8(mx_scale_bytes(cols, rows, block, block_rows, sfmt), dev)
+    st = load().mx_quantize(_ptr(x), rows, cols, block, block_rows, elem, sfmt, layout,
+                            _ptr(q_row) if row else None, _ptr(s_row) if row else None,
+                            _ptr(q_col) if col else None, _ptr(s_col) if col else None, _stream(stream))
+    _check(st, "mx_quantize")
+    return (q_row if row else None, s_row if row else None, q_col if col else None, s_col if col else None)
+
+
+def nvfp4_quantize(x: torch.Tensor, q_packed=None, s_ue4m3=None, gscale=None, workspace=None, stream=None):
+    """NVFP4 two-level quantization of bf16 x[rows][cols] (include/mx.h, nvfp4_quantize).
+    Returns (q_packed [rows][cols/2] u8, s_ue4m3 flat u8 in the NVFP4 GEMM layout,
+    gscale float[1])."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    if q_packed is None:
+        q_packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+    if s_ue4m3 is None:
+        s_ue4m3 = _u8(mx_scale_bytes(rows, cols, 16, 1, SCALE_UE4M3), dev)
+    if gscale is None:
+        gscale = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _u8(max(16, nvfp4_workspace_bytes(rows, cols)), dev)
+    st = load().nvfp4_quantize(_ptr(x), rows, cols, _ptr(q_packed), _ptr(s_ue4m3), _ptr(gscale),
+                               _ptr(workspace), _stream(stream))
+    _check(st, "nvfp4_quantize")
+    return q_packed, s_ue4m3, gscale
+
+
+# ------------------------------------------------------------------ GEMMs
+def _out(M, N, out_dtype, out, dev):
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32, device=dev)
+    return out, out.stride(0)
+
+
+def mx_gemm(qa, sa, ea, qb, sb, eb, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):
+    """C[m][n] = sum_b sA sB sum_i qA qB (MXFP8, include/mx.h mx_gemm)."""
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().mx_gemm(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, M, N, K, out.data_ptr(), out_dtype, ldc,
+                        _stream(stream))
+    _check(st, "mx_gemm")
+    return out
+
+
+def nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=OUT_F32, out=None, stream=None):
+    """C = gA gB sum_b sA sB sum_i qA qB (NVFP4, include/mx.h nvfp4_gemm)."""
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().nvfp4_gemm(_ptr(qa), _ptr(sa), _ptr(ga), _ptr(qb), _ptr(sb), _ptr(gb), M, N, K, out.data_ptr(),
+                           out_dtype, ldc, _stream(stream))
+    _check(st, "nvfp4_gemm")
+    return out
+
+
+def fp8_blockwise_gemm(qa, sa, qb, sb, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):
+    """DeepSeek FP8 GEMM with FP32 promotion every 128 of K (include/mx.h)."""
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().fp8_blockwise_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, N, K, out.data_ptr(), out_dtype, ldc,
+                                   _stream(stream))
+    _check(st, "fp8_blockwise_gemm")
+    return out
+
+
+def mx_check(stream=None) -> int:
+    """Synchronize the stream and return the library's device status (MX_OK / MX_ERR_TIMEOUT / ...)."""
+    return int(load().mx_check(_stream(stream)))
+
+
+def num_sms() -> int:
+    return int(load().mx_num_sms())

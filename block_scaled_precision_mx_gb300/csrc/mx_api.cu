@@ -1,0 +1,316 @@
+// mx_api.cu -- the C ABI declared in include/mx.h: host-side validation, TMA descriptor
+// encoding and kernel launches.  This is the only translation unit of libmxgb.so; the kernels
+// are included from the .cuh files so that the device error word needs no separate linking.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mx.h"
+#include "mx_device.cuh"
+#include "mx_gemm.cuh"
+#include "mx_quantize.cuh"
+
+using namespace mxgb;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+mx_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D byte tensor [rows][row_bytes], box 128 bytes x box_rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- device properties
+struct DevInfo {
+  int sms = 0;
+};
+DevInfo g_dev[64];
+int g_last_sms = 0;
+
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (g_dev[dev].sms == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_dev[dev].sms = n;
+  }
+  g_last_sms = g_dev[dev].sms;
+  return g_dev[dev].sms;
+}
+
+// ---------------------------------------------------------------- GEMM launch
+template <int KIND, int BN, bool OUT_BF16>
+mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
+  using Cfg = GemmCfg<KIND, BN>;
+  auto kern = bs_gemm_kernel<KIND, BN, OUT_BF16>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+      return MX_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::BM)) return MX_ERR_CUDA;
+  if (!make_tmap(&tb, qb, args.N, kbytes, BN)) return MX_ERR_CUDA;
+  const int sms = device_sms();
+  if (sms <= 0) return MX_ERR_CUDA;
+  const int tiles = (args.M / Cfg::BM) * (args.N / BN);
+  const int grid = tiles < sms ? tiles : sms;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, args);
+  return launch_status();
+}
+
+bool gemm_shape_ok(int64_t M, int64_t N, int64_t K, int64_t kmult, int64_t ldc, mx_out od) {
+  if (M <= 0 || N <= 0 || K <= 0) return false;
+  if (M % 128 || N % 128 || K % kmult) return false;
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return false;
+  if (ldc < N || ldc % 8) return false;
+  if (od != MX_OUT_F32 && od != MX_OUT_BF16) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mx_abi_version(void) { return kAbiVersion; }
+
+const char* mx_status_string(mx_status s) {
+  switch (s) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+    case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+  }
+  return "MX_ERR_UNKNOWN";
+}
+
+int mx_num_sms(void) { return g_last_sms; }
+
+size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_scale_fmt sfmt) {
+  if (rows <= 0 || cols <= 0) return 0;
+  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0) return static_cast<size_t>(rows * (cols / 32));
+  if (block == 16 && block_rows == 1 && sfmt == MX_SCALE_UE4M3) return static_cast<size_t>(rows * (cols / 16));
+  if (block == 128 && block_rows == 1 && sfmt == MX_SCALE_FP32) return static_cast<size_t>(4 * rows * (cols / 128));
+  if (block == 128 && block_rows == 128 && sfmt == MX_SCALE_FP32)
+    return static_cast<size_t>(4 * (rows / 128) * (cols / 128));
+  return 0;
+}
+
+mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int block_rows, mx_elem elem,
+                      mx_scale_fmt sfmt, mx_layout layout, void* q_row, void* s_row, void* q_col, void* s_col,
+                      void* stream) {
+  if (!x || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MX_ERR_INVALID_ARG;
+  if (rows > (1ll << 31) || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
+  if (elem != MX_E4M3 && elem != MX_E5M2 && elem != MX_E2M1) return MX_ERR_INVALID_ARG;
+  if (sfmt != MX_SCALE_E8M0 && sfmt != MX_SCALE_UE4M3 && sfmt != MX_SCALE_FP32) return MX_ERR_INVALID_ARG;
+  if (layout != MX_ROWWISE && layout != MX_COLWISE && layout != MX_BOTH) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16)) return MX_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  const bool row = (layout & MX_ROWWISE) != 0, col = (layout & MX_COLWISE) != 0;
+
+  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0 && (elem == MX_E4M3 || elem == MX_E5M2)) {
+    if (row && (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 16))) return MX_ERR_INVALID_ARG;
+    if (col && (!q_col || !s_col || !aligned(q_col, 16) || !aligned(s_col, 16))) return MX_ERR_INVALID_ARG;
+    const int64_t tiles = (rows / 128) * (cols / 128);
+    if (tiles > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    auto* qr = static_cast<uint8_t*>(q_row);
+    auto* sr = static_cast<uint8_t*>(s_row);
+    auto* qc = static_cast<uint8_t*>(q_col);
+    auto* sc = static_cast<uint8_t*>(s_col);
+    const dim3 grid(static_cast<unsigned>(tiles));
+#define MXQ(E, R, C) mx_quantize_kernel<E, R, C><<<grid, 256, 0, st>>>(xb, rows, cols, qr, sr, qc, sc)
+    if (elem == MX_E4M3) {
+      if (row && col) MXQ(0, true, true);
+      else if (row) MXQ(0, true, false);
+      else MXQ(0, false, true);
+    } else {
+      if (row && col) MXQ(1, true, true);
+      else if (row) MXQ(1, true, false);
+      else MXQ(1, false, true);
+    }
+#undef MXQ
+    return launch_status();
+  }
+  if (block == 128 && sfmt == MX_SCALE_FP32 && elem == MX_E4M3 && layout == MX_ROWWISE &&
+      (block_rows == 1 || block_rows == 128)) {
+    if (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 4)) return MX_ERR_INVALID_ARG;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (block_rows == 1) {
+      const int64_t ctas = (rows / 32) * (cols / 128);
+      if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+      ds_quantize_1x128_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(xb, rows, cols,
+                                                                            static_cast<uint8_t*>(q_row),
+                                                                            static_cast<float*>(s_row));
+    } else {
+      const int64_t ctas = (rows / 128) * (cols / 128);
+      if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+      ds_quantize_128x128_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(xb, rows, cols,
+                                                                              static_cast<uint8_t*>(q_row),
+                                                                              static_cast<float*>(s_row));
+    }
+    return launch_status();
+  }
+  return MX_ERR_UNSUPPORTED;
+}
+
+mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb, int64_t M,
+                  int64_t N, int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !out) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16))
+    return MX_ERR_INVALID_ARG;
+  if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
+    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
+    return MX_ERR_INVALID_ARG;
+  }
+  GemmArgs a{};
+  a.sfa = static_cast<const uint8_t*>(sa);
+  a.sfb = static_cast<const uint8_t*>(sb);
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  const bool bn256 = (N % 256) == 0;
+  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 128, bn256 ? 256 : 128, 1);
+  cudaStream_t st = as_stream(stream);
+  const bool bf = out_dtype == MX_OUT_BF16;
+  if (bn256) return bf ? launch_gemm<kMxf8, 256, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 256, false>(qa, qb, K, a, st);
+  return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
+}
+
+size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols) {
+  (void)rows;
+  (void)cols;
+  return 16;
+}
+
+mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* q_packed, void* s_ue4m3, float* gscale,
+                         void* workspace, void* stream) {
+  if (!x || !q_packed || !s_ue4m3 || !gscale || !workspace) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || rows % 128 || cols % 64) return MX_ERR_INVALID_ARG;
+  if (rows > (1ll << 31) || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q_packed, 16) || !aligned(s_ue4m3, 16) || !aligned(gscale, 4) ||
+      !aligned(workspace, 16))
+    return MX_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  auto* amax = static_cast<unsigned int*>(workspace);
+  if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), st) != cudaSuccess) return MX_ERR_CUDA;
+  const int sms = device_sms();
+  if (sms <= 0) return MX_ERR_CUDA;
+  const int64_t nvec = rows * cols / 8;
+  int64_t grid1 = (nvec + 255) / 256;
+  if (grid1 > 8ll * sms) grid1 = 8ll * sms;
+  nvfp4_amax_kernel<<<static_cast<unsigned>(grid1), 256, 0, st>>>(static_cast<const uint16_t*>(x), nvec, amax);
+  if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
+  const int64_t ctas = (rows / 32) * ((cols + 127) / 128);
+  if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(static_cast<const uint16_t*>(x), rows, cols,
+                                                                      static_cast<uint8_t*>(q_packed),
+                                                                      static_cast<uint8_t*>(s_ue4m3), gscale, amax);
+  return launch_status();
+}
+
+mx_status nvfp4_gemm(const void* qa, const void* sa, const float* ga, const void* qb, const void* sb, const float* gb,
+                     int64_t M, int64_t N, int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !ga || !qb || !sb || !gb || !out) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 256, ldc, out_dtype)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16) ||
+      !aligned(ga, 4) || !aligned(gb, 4))
+    return MX_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.sfa = static_cast<const uint8_t*>(sa);
+  a.sfb = static_cast<const uint8_t*>(sb);
+  a.ga = ga;
+  a.gb = gb;
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  const bool bn256 = (N % 256) == 0;
+  a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 0);
+  cudaStream_t st = as_stream(stream);
+  const bool bf = out_dtype == MX_OUT_BF16;
+  const int64_t kb = K / 2;
+  if (bn256) return bf ? launch_gemm<kNvf4, 256, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 256, false>(qa, qb, kb, a, st);
+  return bf ? launch_gemm<kNvf4, 128, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 128, false>(qa, qb, kb, a, st);
+}
+
+mx_status fp8_blockwise_gemm(const void* qa, const float* sa, const void* qb, const float* sb, int64_t M, int64_t N,
+                             int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !out) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 4) || !aligned(sb, 4) || !aligned(out, 16))
+    return MX_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.dsa = sa;
+  a.dsb = sb;
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.idesc = make_idesc_f8f6f4(0u, 0u, 128, 128);
+  cudaStream_t st = as_stream(stream);
+  if (out_dtype == MX_OUT_BF16) return launch_gemm<kDsF8, 128, true>(qa, qb, K, a, st);
+  return launch_gemm<kDsF8, 128, false>(qa, qb, K, a, st);
+}
+
+mx_status mx_check(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MX_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_mx_error_word, sizeof(word)) != cudaSuccess) return MX_ERR_CUDA;
+  if (word) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_mx_error_word, &zero, sizeof(zero)) != cudaSuccess) return MX_ERR_CUDA;
+    return MX_ERR_TIMEOUT;
+  }
+  return MX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,380 @@
+// mx_gemm.cuh -- block-scaled GEMMs on the 5th-generation tensor cores (tcgen05) of sm_103a.
+//
+// One warp-specialized, persistent kernel skeleton serves three products, all of the form
+// C[m][n] = sum_k A[m][k] B[n][k] with K-contiguous operands:
+//   kMxf8 : MXFP8 -- tcgen05.mma kind::mxf8f6f4.block_scale, one E8M0 scale per 32 of K for
+//           each operand; the tensor core applies sA_b * sB_b to every 32-block partial sum.
+//           "MXFP8 on SM120: software support" (xuesongtap.github.io), sec 0.3.
+//   kNvf4 : NVFP4 -- kind::mxf4nvf4.block_scale.scale_vec::4X, one E4M3 scale per 16 of K;
+//           the FP32 per-tensor scales multiply the result in the epilogue.
+//           "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 7.3 (four-step pipeline:
+//           narrow products, per-16 partial sums, times block scales, epilogue times the
+//           global scale) and sec 7.4 (scales of both operands).
+//   kDsF8 : DeepSeek FP8 -- kind::f8f6f4 over one 128-wide k-block at a time into one of two
+//           TMEM accumulators; epilogue warps promote every k-block into FP32 registers as
+//           acc += sA[kb][m] * sB[n/128][kb] * P while the tensor core fills the other buffer.
+//           "Why FP8 training is stable" (magicnetworld.com), sec 6.3 (N_C = 128 promotion,
+//           overlapped with MMA issue).
+//
+// Roles (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: A/B tiles (128-byte swizzled rows, one row = 128 B of K) and
+//               scale chunks (bulk copies) into a ring of smem stages.
+//   warp 1      TMEM allocation + single-thread MMA issue: tcgen05.cp of the stage's scale
+//               chunks into TMEM, then 4 tcgen05.mma (32 bytes of K each) per stage.
+//   warps 2..   epilogue: tcgen05.ld of the accumulator, scale / convert, vector stores.
+// Stages are handed over with mbarriers (TMA complete_tx -> MMA; tcgen05.commit -> producer;
+// tcgen05.commit -> epilogue; epilogue arrivals -> MMA).  Every wait is bounded.
+#pragma once
+
+#include "mx_device.cuh"
+
+namespace mxgb {
+
+enum GemmKind : int { kMxf8 = 0, kNvf4 = 1, kDsF8 = 2 };
+
+constexpr int kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per CTA
+
+template <int KIND, int BN>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int KBYTES = 128;  // bytes of K per stage: one 128-byte swizzle row
+  static constexpr int K_ELEMS = (KIND == kNvf4) ? 256 : 128;
+  static constexpr int A_BYTES = BM * KBYTES;
+  static constexpr int B_BYTES = BN * KBYTES;
+  static constexpr int RC = BN / 128;  // 128-row scale chunks of B per tile
+  static constexpr int SFA_BYTES = (KIND == kMxf8) ? 512 : (KIND == kNvf4 ? 2048 : 0);
+  static constexpr int SFB_BYTES = SFA_BYTES * RC;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int NUM_MMA = KBYTES / 32;  // tcgen05.mma per stage (32 bytes of K each)
+  // TMEM columns
+  static constexpr int ACC_COLS = (KIND == kDsF8) ? 2 * BN : BN;
+  static constexpr int SFA_COL = ACC_COLS;
+  static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : (KIND == kNvf4 ? 16 : 0);
+  static constexpr int SFB_COL = SFA_COL + SFA_COLS;
+  static constexpr int SFB_COLS = (KIND == kMxf8) ? 4 * RC : (KIND == kNvf4 ? 16 * RC : 0);
+  static constexpr int USED_COLS = SFB_COL + SFB_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
+                                   : USED_COLS <= 256 ? 256 : 512;
+  static constexpr int NUM_EPI_WARPS = (KIND == kDsF8) ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+  static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+  static_assert(STAGES >= 2, "not enough shared memory for two stages");
+  static_assert(USED_COLS <= 512, "TMEM overflow");
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "bad BN");
+};
+
+struct GemmArgs {
+  const uint8_t* sfa;  // MX / NV scale chunks of A
+  const uint8_t* sfb;
+  const float* dsa;  // DeepSeek: float[K/128][M]
+  const float* dsb;  // DeepSeek: float[N/128][K/128]
+  const float* ga;   // NVFP4 global scales
+  const float* gb;
+  void* out;
+  int64_t ldc;
+  int M, N, K;  // K in elements
+  uint32_t idesc;
+};
+
+// Tile order: bands of 16 m-blocks; inside a band, m runs fastest, so the CTAs of one wave
+// share a few B tiles and a band of A tiles in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_mb, int num_nb, int& mb, int& nb) {
+  constexpr int G = 16;
+  const int band_tiles = G * num_nb;
+  const int band = tile / band_tiles;
+  const int in = tile - band * band_tiles;
+  const int mb0 = band * G;
+  const int gm = min(G, num_mb - mb0);
+  nb = in / gm;
+  mb = mb0 + (in - nb * gm);
+}
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_row32(void* out, int64_t ldc, int64_t row, int64_t col, const float* v) {
+  if (OUT_BF16) {
+    uint32_t p[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      p[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + row * ldc + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + row * ldc + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+template <int KIND, int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
+    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+  using Cfg = GemmCfg<KIND, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + Cfg::STAGES * Cfg::A_BYTES;
+  uint8_t* sSFA = sB + Cfg::STAGES * Cfg::B_BYTES;
+  uint8_t* sSFB = sSFA + Cfg::STAGES * Cfg::SFA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + Cfg::STAGES;
+  uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;   // [2]
+  uint64_t* tempty_bar = bars + 2 * Cfg::STAGES + 2;  // [2]
+  uint64_t* drain_bar = bars + 2 * Cfg::STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_mb = args.M / Cfg::BM;
+  const int num_nb = args.N / BN;
+  const int num_tiles = num_mb * num_nb;
+  const int num_kt = args.K / Cfg::K_ELEMS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], Cfg::EPI_THREADS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      const int64_t kchunks_mx = args.K / 128;  // MX scale chunks per 128 rows
+      const int64_t kchunks_nv = args.K / 64;   // NV scale chunks per 128 rows
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_mb, num_nb, mb, nb);
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
+          tma_load_2d(sA + stage * Cfg::A_BYTES, &tmA, &full_bar[stage], kt * Cfg::KBYTES, mb * Cfg::BM);
+          tma_load_2d(sB + stage * Cfg::B_BYTES, &tmB, &full_bar[stage], kt * Cfg::KBYTES, nb * BN);
+          if (KIND == kMxf8) {
+            bulk_load(sSFA + stage * Cfg::SFA_BYTES, args.sfa + (mb * kchunks_mx + kt) * 512, 512,
+                      &full_bar[stage]);
+#pragma unroll
+            for (int rc = 0; rc < Cfg::RC; ++rc)
+              bulk_load(sSFB + stage * Cfg::SFB_BYTES + rc * 512,
+                        args.sfb + ((static_cast<int64_t>(nb) * Cfg::RC + rc) * kchunks_mx + kt) * 512, 512,
+                        &full_bar[stage]);
+          } else if (KIND == kNvf4) {
+            bulk_load(sSFA + stage * Cfg::SFA_BYTES, args.sfa + (mb * kchunks_nv + 4ll * kt) * 512, 2048,
+                      &full_bar[stage]);
+#pragma unroll
+            for (int rc = 0; rc < Cfg::RC; ++rc)
+              bulk_load(sSFB + stage * Cfg::SFB_BYTES + rc * 2048,
+                        args.sfb + ((static_cast<int64_t>(nb) * Cfg::RC + rc) * kchunks_nv + 4ll * kt) * 512, 2048,
+                        &full_bar[stage]);
+          }
+          ++issued;
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: every copy this thread issued must have landed before the CTA exits
+      for (int s = 0; s < Cfg::STAGES; ++s) {
+        if (issued > s) {
+          const long last = s + ((issued - 1 - s) / Cfg::STAGES) * Cfg::STAGES;
+          mbar_wait(&full_bar[s], static_cast<uint32_t>((last / Cfg::STAGES) & 1), abort_flag, kSiteDrain);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_it = 0;  // accumulator hand-overs so far
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (KIND != kDsF8) {
+          if (!mbar_wait(&tempty_bar[0], (acc_it & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) break;
+          tc_fence_after();
+        }
+        for (int kt = 0; kt < num_kt; ++kt) {
+          uint32_t d_tmem = tmem_base;
+          if (KIND == kDsF8) {
+            const uint32_t b = acc_it & 1;
+            if (!mbar_wait(&tempty_bar[b], ((acc_it >> 1) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + b * BN;
+          }
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * Cfg::A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_BYTES);
+          if (KIND == kMxf8) {
+            tmem_cp_32x128b_warpx4(tmem_base + Cfg::SFA_COL,
+                                   make_smem_desc(smem_u32(sSFA + stage * Cfg::SFA_BYTES), 0, 128, kSwizzleNone));
+#pragma unroll
+            for (int rc = 0; rc < Cfg::RC; ++rc)
+              tmem_cp_32x128b_warpx4(
+                  tmem_base + Cfg::SFB_COL + 4 * rc,
+                  make_smem_desc(smem_u32(sSFB + stage * Cfg::SFB_BYTES + rc * 512), 0, 128, kSwizzleNone));
+          } else if (KIND == kNvf4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_32x128b_warpx4(
+                  tmem_base + Cfg::SFA_COL + 4 * j,
+                  make_smem_desc(smem_u32(sSFA + stage * Cfg::SFA_BYTES + j * 512), 0, 128, kSwizzleNone));
+#pragma unroll
+              for (int rc = 0; rc < Cfg::RC; ++rc)
+                tmem_cp_32x128b_warpx4(tmem_base + Cfg::SFB_COL + j * 4 * Cfg::RC + 4 * rc,
+                                       make_smem_desc(smem_u32(sSFB + stage * Cfg::SFB_BYTES + rc * 2048 + j * 512),
+                                                      0, 128, kSwizzleNone));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < Cfg::NUM_MMA; ++j) {
+            const uint64_t adesc = make_smem_desc(a_addr + j * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = make_smem_desc(b_addr + j * 32, 16, 1024, kSwizzle128B);
+            if (KIND == kMxf8) {
+              umma_mxf8f6f4(d_tmem, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), tmem_base + Cfg::SFA_COL,
+                            tmem_base + Cfg::SFB_COL, (kt > 0 || j > 0) ? 1u : 0u);
+            } else if (KIND == kNvf4) {
+              umma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, tmem_base + Cfg::SFA_COL + 4 * j,
+                            tmem_base + Cfg::SFB_COL + j * 4 * Cfg::RC, (kt > 0 || j > 0) ? 1u : 0u);
+            } else {
+              umma_f8f6f4(d_tmem, adesc, bdesc, args.idesc, j > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty_bar[stage]);  // frees the smem stage once these MMAs are done
+          if (KIND == kDsF8) {
+            umma_commit(&tfull_bar[acc_it & 1]);  // one k-block ready for promotion
+            ++acc_it;
+          }
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (KIND != kDsF8 && ok) {
+          umma_commit(&tfull_bar[0]);
+          ++acc_it;
+        }
+      }
+      // drain: all MMAs issued by this thread complete before TMEM is released
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t acc_it = 0;
+    if (KIND != kDsF8) {
+      float gscale = 1.0f;
+      if (KIND == kNvf4) gscale = __fmul_rn(*args.ga, *args.gb);
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_mb, num_nb, mb, nb);
+        bool ok = mbar_wait(&tfull_bar[0], acc_it & 1, abort_flag, kSiteEpiTmemFull);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + c * 32, r);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[i]), gscale)
+                                                              : __uint_as_float(r[i]);
+          store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + c * 32, v);
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty_bar[0]);
+        ++acc_it;
+      }
+    } else {
+      // DeepSeek promotion: this warp owns rows q*32.. and columns [half*64, half*64+64)
+      const int half = (warp - 2) >> 2;
+      const int64_t kbs = args.K / 128;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_mb, num_nb, mb, nb);
+        const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
+        float acc[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        for (int kt = 0; kt < num_kt; ++kt) {
+          const uint32_t b = acc_it & 1;
+          ok = mbar_wait(&tfull_bar[b], (acc_it >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float s = __fmul_rn(args.dsa[static_cast<int64_t>(kt) * args.M + row],
+                                    args.dsb[static_cast<int64_t>(nb) * (BN / 128) * kbs + kt]);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64 + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 32 + i]);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty_bar[b]);
+          ++acc_it;
+        }
+        if (!ok) break;
+        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64, acc);
+        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64 + 32, acc + 32);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+}  // namespace mxgb

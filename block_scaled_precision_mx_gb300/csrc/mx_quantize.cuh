@@ -1,0 +1,334 @@
+// mx_quantize.cuh -- bandwidth-bound quantizer kernels for sm_103a.
+//
+//  * mx_quantize_kernel: MX (OCP) block quantization of a bf16 matrix, row-wise (1x32 blocks
+//    along the row) and column-wise (32x1 blocks down each column, stored transposed) from a
+//    single read of the input.  "MXFP8 on SM120: software support" (xuesongtap.github.io),
+//    sec 0.1 (block format, E8M0 scale, q = Q(x/s)) and sec 1.2 (a transpose needs its own
+//    blocks, scales and codes).
+//  * ds_quantize_1x128_kernel / ds_quantize_128x128_kernel: DeepSeek fine-grained FP8 with
+//    FP32 scales s = amax/448.  "Why FP8 training is stable" (magicnetworld.com), sec 4 and 5.
+//  * nvfp4_amax_kernel / nvfp4_quantize_kernel: NVFP4 two-level quantization.
+//    "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 5.4 and 5.6.
+//
+// Every kernel streams its input once with 128-bit loads, reduces block maxima in registers
+// (warp shuffles where a block spans lanes), and writes codes with vector stores.  Scales are
+// written in the 512-byte chunk layout the GEMMs read (see include/mx.h).
+#pragma once
+
+#include "mx_device.cuh"
+
+namespace mxgb {
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// offset of (row i, block j) inside a 512-byte scale chunk (128 rows x 4 blocks)
+__device__ __forceinline__ int chunk_offset(int i, int j) { return (i & 31) * 16 + (i >> 5) * 4 + j; }
+
+// ---------------------------------------------------------------------------------------------
+// MX quantize.  One CTA = one 128 x 128 tile of the input (256 threads).  The tile maps to
+// exactly one 512-byte row-wise scale chunk and one column-wise scale chunk.
+// ---------------------------------------------------------------------------------------------
+template <int ELEM>  // 0 = E4M3 (emax 8), 1 = E5M2 (emax 15)
+struct MxElem;
+template <>
+struct MxElem<0> {
+  static constexpr int emax = 8;
+  __device__ static uint32_t cvt2(float lo, float hi) { return cvt_e4m3x2(lo, hi); }
+};
+template <>
+struct MxElem<1> {
+  static constexpr int emax = 15;
+  __device__ static uint32_t cvt2(float lo, float hi) { return cvt_e5m2x2(lo, hi); }
+};
+
+// E8M0 scale byte from the largest |x| bit pattern (bf16 bits & 0x7fff) of a finite block:
+// k = floor(log2 amax) - emax clamped to >= -127; byte = k + 127 = max(expfield - emax, 0).
+template <int ELEM>
+__device__ __forceinline__ uint32_t mx_scale_byte(uint32_t amax_bits) {
+  const int e = static_cast<int>(amax_bits >> 7);  // biased exponent (0 for zero / subnormal)
+  const int c = e - MxElem<ELEM>::emax;
+  return c > 0 ? static_cast<uint32_t>(c) : 0u;
+}
+
+// 2^-k for scale byte c (k = c - 127): an FP32 with exponent field 254 - c (always normal).
+__device__ __forceinline__ float mx_inv_scale(uint32_t c) { return __uint_as_float((254u - c) << 23); }
+
+// Quantize 8 bf16 values (one uint4) with inverse scale `inv`; returns 8 packed codes.
+template <int ELEM>
+__device__ __forceinline__ uint2 mx_codes8(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __fmul_rn(bf16_bits_to_float(w[i] & 0xFFFFu), inv);
+    const float hi = __fmul_rn(bf16_bits_to_float(w[i] >> 16), inv);
+    p[i] = MxElem<ELEM>::cvt2(lo, hi);
+  }
+  return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+__device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
+  uint32_t m = 0;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = max(m, w[i] & 0x7FFFu);
+    m = max(m, (w[i] >> 16) & 0x7FFFu);
+  }
+  return m;
+}
+
+template <int ELEM, bool ROW, bool COL>
+__global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                          int64_t cols, uint8_t* __restrict__ q_row,
+                                                          uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
+                                                          uint8_t* __restrict__ s_col) {
+  __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 1];  // 128 rows x 128 bf16 (as bf16x2 words)
+  __shared__ __align__(16) uint8_t srow[512];
+  __shared__ __align__(16) uint8_t scol[512];
+
+  const int64_t tiles_c = cols >> 7;
+  const int64_t tr = blockIdx.x / tiles_c;
+  const int64_t tc = blockIdx.x % tiles_c;
+  const int t = threadIdx.x;
+  const int lc = t & 15;     // 16 threads per row, 8 bf16 (one uint4) each
+  const int r0 = t >> 4;     // rows r0 + 16*i
+
+  const uint16_t* xt = x + (tr * 128) * cols + tc * 128;
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(xt + static_cast<int64_t>(r0 + 16 * i) * cols + lc * 8);
+
+  if (COL) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4*>(&tile[(r0 + 16 * i) * 64 + lc * 4]) = v[i];
+  }
+
+  if (ROW) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + 16 * i;
+      uint32_t m = absmax_bits8(v[i]);
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      uint2 codes;
+      uint32_t sbyte;
+      if (m >= 0x7F80u) {  // NaN or Inf in the block
+        sbyte = 0xFF;
+        codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      } else {
+        sbyte = mx_scale_byte<ELEM>(m);
+        codes = mx_codes8<ELEM>(v[i], mx_inv_scale(sbyte));
+      }
+      *reinterpret_cast<uint2*>(q_row + (tr * 128 + r) * cols + tc * 128 + lc * 8) = codes;
+      if ((lc & 3) == 0) srow[chunk_offset(r, lc >> 2)] = static_cast<uint8_t>(sbyte);
+    }
+  }
+
+  if (COL) {
+    __syncthreads();
+    // thread -> (column pair p, row block rb): reads one bf16x2 word per row of its block
+    const int p = t & 63;
+    const int rb = t >> 6;
+    uint32_t w[32];
+    uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      w[r] = tile[(rb * 32 + r) * 64 + p];
+      m0 = max(m0, w[r] & 0x7FFFu);
+      m1 = max(m1, (w[r] >> 16) & 0x7FFFu);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t m = h ? m1 : m0;
+      const int c = 2 * p + h;  // column inside the tile = row of the transposed tile
+      uint32_t packed[8];
+      uint32_t sbyte;
+      if (m >= 0x7F80u) {
+        sbyte = 0xFF;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) packed[j] = 0x7F7F7F7Fu;
+      } else {
+        sbyte = mx_scale_byte<ELEM>(m);
+        const float inv = mx_inv_scale(sbyte);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int sh = h ? 16 : 0;
+          const float f0 = __fmul_rn(bf16_bits_to_float((w[4 * j + 0] >> sh) & 0xFFFFu), inv);
+          const float f1 = __fmul_rn(bf16_bits_to_float((w[4 * j + 1] >> sh) & 0xFFFFu), inv);
+          const float f2 = __fmul_rn(bf16_bits_to_float((w[4 * j + 2] >> sh) & 0xFFFFu), inv);
+          const float f3 = __fmul_rn(bf16_bits_to_float((w[4 * j + 3] >> sh) & 0xFFFFu), inv);
+          packed[j] = MxElem<ELEM>::cvt2(f0, f1) | (MxElem<ELEM>::cvt2(f2, f3) << 16);
+        }
+      }
+      uint8_t* dst = q_col + (tc * 128 + c) * rows + tr * 128 + rb * 32;
+      reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      scol[chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
+    }
+  }
+
+  __syncthreads();
+  if (t < 32) {
+    if (ROW) {
+      uint8_t* dst = s_row + (tr * tiles_c + tc) * 512;
+      reinterpret_cast<uint4*>(dst)[t] = reinterpret_cast<const uint4*>(srow)[t];
+    }
+  } else if (t < 64) {
+    if (COL) {
+      const int64_t tiles_r = rows >> 7;
+      uint8_t* dst = s_col + (tc * tiles_r + tr) * 512;
+      reinterpret_cast<uint4*>(dst)[t - 32] = reinterpret_cast<const uint4*>(scol)[t - 32];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// DeepSeek 1x128: one warp per (row, 128-block); lane holds 4 consecutive bf16.
+// s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored [K/128][rows].
+// CTA = 8 warps = 8 consecutive rows of the same k-block, 4 iterations -> 32 rows.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t cols, uint8_t* __restrict__ q,
+                                                                float* __restrict__ s) {
+  const int64_t kb_count = cols >> 7;
+  const int64_t kb = blockIdx.x % kb_count;
+  const int64_t rgrp = blockIdx.x / kb_count;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int64_t r = rgrp * 32 + it * 8 + warp;
+    const uint2 v = *reinterpret_cast<const uint2*>(x + r * cols + kb * 128 + lane * 4);
+    const uint32_t w[2] = {v.x, v.y};
+    uint32_t m = max(max(w[0] & 0x7FFFu, (w[0] >> 16) & 0x7FFFu), max(w[1] & 0x7FFFu, (w[1] >> 16) & 0x7FFFu));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float amax = bf16_bits_to_float(m);
+    const float sc = (m == 0) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float f0 = __fdiv_rn(bf16_bits_to_float(w[0] & 0xFFFFu), sc);
+    const float f1 = __fdiv_rn(bf16_bits_to_float(w[0] >> 16), sc);
+    const float f2 = __fdiv_rn(bf16_bits_to_float(w[1] & 0xFFFFu), sc);
+    const float f3 = __fdiv_rn(bf16_bits_to_float(w[1] >> 16), sc);
+    *reinterpret_cast<uint32_t*>(q + r * cols + kb * 128 + lane * 4) = cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16);
+    if (lane == 0) s[kb * rows + r] = sc;
+  }
+}
+
+// DeepSeek 128x128 weight blocks: one CTA per block; 256 threads x 64 elements in registers.
+__global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                  int64_t cols, uint8_t* __restrict__ q,
+                                                                  float* __restrict__ s) {
+  __shared__ uint32_t wmax[8];
+  const int64_t nbc = cols >> 7;
+  const int64_t br = blockIdx.x / nbc, bc = blockIdx.x % nbc;
+  const int t = threadIdx.x;
+  const int lc = t & 15, r0 = t >> 4;
+  const uint16_t* xb = x + (br * 128) * cols + bc * 128;
+  uint4 v[8];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = ld_stream_v4(xb + static_cast<int64_t>(r0 + 16 * i) * cols + lc * 8);
+    m = max(m, absmax_bits8(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((t & 31) == 0) wmax[t >> 5] = m;
+  __syncthreads();
+  m = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
+  const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      p[j] = cvt_e4m3x2(__fdiv_rn(bf16_bits_to_float(w[j] & 0xFFFFu), sc),
+                        __fdiv_rn(bf16_bits_to_float(w[j] >> 16), sc));
+    *reinterpret_cast<uint2*>(q + (br * 128 + r0 + 16 * i) * cols + bc * 128 + lc * 8) =
+        make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+  }
+  if (t == 0) s[br * nbc + bc] = sc;
+}
+
+// ---------------------------------------------------------------------------------------------
+// NVFP4 pass 1: global amax (as FP32 bits, atomicMax; non-negative floats order as integers).
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restrict__ x, int64_t n_vec8,
+                                                         unsigned int* __restrict__ amax_bits) {
+  __shared__ uint32_t wmax[8];
+  uint32_t m = 0;
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n_vec8; i += static_cast<int64_t>(gridDim.x) * 256)
+    m = max(m, absmax_bits8(ld_stream_v4(x + i * 8)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
+    atomicMax(amax_bits, m << 16);  // bf16 bits -> FP32 bits
+  }
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t code) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\t"
+      "cvt.u16.u32 t, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(code));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// NVFP4 pass 2.  CTA = 32 rows x 128 columns; thread = one 16-element block.
+__global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                             int64_t cols, uint8_t* __restrict__ qp,
+                                                             uint8_t* __restrict__ sf, float* __restrict__ gscale,
+                                                             const unsigned int* __restrict__ amax_bits) {
+  // column tiles of 128; the last one may be half full (cols % 128 == 64)
+  const int64_t tiles_c = (cols + 127) >> 7;
+  const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+  const int t = threadIdx.x;
+  const int64_t r = tr * 32 + (t >> 3);
+  const int64_t c = tc * 128 + (t & 7) * 16;
+  if (c >= cols) return;
+  const float amax = __uint_as_float(*amax_bits);
+  const float sg = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && t == 0) *gscale = sg;
+
+  const uint4 v0 = ld_stream_v4(x + r * cols + c);
+  const uint4 v1 = ld_stream_v4(x + r * cols + c + 8);
+  const uint32_t bm = max(absmax_bits8(v0), absmax_bits8(v1));
+  const float bamax = bf16_bits_to_float(bm);
+  const float tq = __fdiv_rn(__fdiv_rn(bamax, 6.0f), sg);
+  const uint32_t scode = cvt_e4m3x2(tq, 0.0f) & 0xFFu;
+  const float s_hat = __fmul_rn(e4m3_to_float(scode), sg);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint32_t lo = 0, hi = 0;
+  if (s_hat != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a = __fdiv_rn(bf16_bits_to_float(w[i] & 0xFFFFu), s_hat);
+      const float b = __fdiv_rn(bf16_bits_to_float(w[i] >> 16), s_hat);
+      const uint32_t byte = cvt_e2m1x2(a, b);
+      if (i < 4) lo |= byte << (8 * i);
+      else hi |= byte << (8 * (i - 4));
+    }
+  }
+  *reinterpret_cast<uint2*>(qp + r * (cols >> 1) + (c >> 1)) = make_uint2(lo, hi);
+  // scale chunk (r / 128, c / 64), 128 rows x 4 blocks of 16
+  const int64_t chunk = (r >> 7) * (cols >> 6) + (c >> 6);
+  sf[chunk * 512 + chunk_offset(static_cast<int>(r & 127), static_cast<int>((c >> 4) & 3))] =
+      static_cast<uint8_t>(scode);
+}
+
+}  // namespace mxgb

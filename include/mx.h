@@ -1,0 +1,182 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) block-scaled quantization and GEMM library
+ * (libmxgb.so).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are CALLER-OWNED DEVICE memory.  No call allocates or frees.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream).  No call synchronizes the host.
+ *  - Matrices are row-major.  A GEMM computes C[m][n] = sum_k A[m][k] * B[n][k]: both code
+ *    operands are K-contiguous ("TN" in column-major BLAS terms).  Column-wise quantized
+ *    copies are stored physically transposed, so fprop, dgrad and wgrad all run as this one
+ *    product:  fprop  Y  = X W^T : A = X row-wise,   B = W row-wise
+ *              dgrad dX  = G W   : A = G row-wise,   B = W column-wise (W^T)
+ *              wgrad dW  = G^T X : A = G column-wise, B = X column-wise
+ *  - Arguments are validated on the host before anything is launched.  A null pointer, a
+ *    shape that is not a multiple of the tile, a misaligned pointer or a bad enum value
+ *    returns MX_ERR_INVALID_ARG; a valid but unimplemented combination returns
+ *    MX_ERR_UNSUPPORTED; a launch failure returns MX_ERR_CUDA.
+ *  - Device-side waits are bounded.  A wait that runs out sets a device error word instead of
+ *    hanging; mx_check() reports it as MX_ERR_TIMEOUT.
+ *
+ * Scale-factor layouts ("GEMM layout", written by the quantizers, read by the GEMMs)
+ *  - MX, E8M0, one scale per 32 consecutive elements along K.  For a code matrix Q[R][K]
+ *    (R % 128 == 0, K % 128 == 0) the R*K/32 scale bytes form 512-byte chunks, one per
+ *    128 rows x 128 elements of K.  Chunk (rb, kc), rb < R/128, kc < K/128, starts at byte
+ *    (rb * (K/128) + kc) * 512.  Inside it, the scale of row 128*rb + i and of 32-block
+ *    4*kc + j is at byte (i % 32) * 16 + (i / 32) * 4 + j.
+ *  - NVFP4, E4M3, one scale per 16 consecutive elements along K: the same 512-byte chunk
+ *    shape, but a chunk covers 128 rows x 64 elements of K (4 blocks of 16); chunk (rb, kc),
+ *    kc < K/64, starts at byte (rb * (K/64) + kc) * 512, in-chunk offset as above.
+ *  - DeepSeek FP32 scales: 1x128 activation tiles are stored k-block-major, s[K/128][R]
+ *    (float), so one k-block's scales for consecutive rows are contiguous; 128x128 weight
+ *    blocks are stored s[R/128][K/128] (float).
+ *  - Packed FP4: element 2i of a row in the low nibble of byte i, element 2i+1 in the high
+ *    nibble.
+ *
+ * Sources (page title and section):
+ *  [MX]  "MXFP8 on SM120: software support" (xuesongtap.github.io): sec 0.1 MX block format,
+ *        E8M0 scale, q = Q_FP8(x / s); sec 0.3 block-scaled dot product; sec 1.1-1.2 TN/NN/NT
+ *        and the fprop/dgrad/wgrad GEMM trio; sec 1.2 row-wise vs column-wise blocks.
+ *  [DS]  "Why FP8 training is stable" (magicnetworld.com): sec 4 s = amax/MAX; sec 5 1x128
+ *        activation tiles and 128x128 weight blocks; sec 6.3 FP32 promotion every N_C = 128.
+ *  [NV]  "NVFP4: high accuracy with 4 bits" (theluyuan.com): sec 5.4 two-level scales;
+ *        sec 5.6 worked example; sec 7.3-7.4 block scale outside the sum, global scale in the
+ *        epilogue.
+ */
+#ifndef MXGB_MX_H_
+#define MXGB_MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,
+  MX_ERR_UNSUPPORTED = 2,
+  MX_ERR_CUDA = 3,
+  MX_ERR_TIMEOUT = 4
+} mx_status;
+
+typedef enum { MX_E4M3 = 0, MX_E5M2 = 1, MX_E2M1 = 2 } mx_elem;
+typedef enum { MX_SCALE_E8M0 = 0, MX_SCALE_UE4M3 = 1, MX_SCALE_FP32 = 2 } mx_scale_fmt;
+typedef enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_BOTH = 3 } mx_layout;
+typedef enum { MX_OUT_F32 = 0, MX_OUT_BF16 = 1 } mx_out;
+
+/* Version of this ABI (bumped on any signature or layout change). */
+int mx_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mx_status_string(mx_status s);
+
+/*
+ * mx_quantize -- block quantization of a bf16 matrix.  [MX] sec 0.1, [DS] sec 4-5.
+ *
+ * x[rows][cols]: bf16, row-major, 16-byte aligned.  Blocks run along cols (the reduction
+ * axis of the consuming GEMM) for the row-wise copy and along rows for the column-wise copy.
+ *
+ * Supported combinations (anything else returns MX_ERR_UNSUPPORTED):
+ *  1. MX: block = 32, block_rows = 1, elem = MX_E4M3 or MX_E5M2, sfmt = MX_SCALE_E8M0,
+ *     layout = ROWWISE, COLWISE or BOTH; rows % 128 == 0, cols % 128 == 0.
+ *     Per block: amax = max |x|; k = clamp(floor(log2 amax) - emax, -127, 127) with emax 8
+ *     (E4M3) or 15 (E5M2), k = -127 when amax == 0; scale byte = k + 127;
+ *     q = RNE-satfinite(x * 2^-k).  A NaN or Inf in a block gives scale 0xFF and all codes
+ *     0x7F.  With BOTH, both copies come from one read of x.
+ *       q_row[rows][cols] u8, s_row: rows*cols/32 bytes in the MX GEMM layout;
+ *       q_col[cols][rows] u8 (transposed), s_col: the MX GEMM layout of that [cols][rows]
+ *       matrix.  Pointers of a copy that is not requested may be NULL.
+ *  2. DeepSeek activations: block = 128, block_rows = 1, elem = MX_E4M3,
+ *     sfmt = MX_SCALE_FP32, layout = ROWWISE; rows % 128 == 0, cols % 128 == 0.
+ *     s = fl32(amax / 448) (1.0 when amax == 0); q = RNE-satfinite(fl32(x / s)).
+ *       q_row[rows][cols] u8, s_row float[cols/128][rows].
+ *  3. DeepSeek weights: block = 128, block_rows = 128, otherwise as 2.
+ *       q_row[rows][cols] u8, s_row float[rows/128][cols/128].
+ *     Inputs for 2 and 3 must be finite.
+ */
+mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int block_rows,
+                      mx_elem elem, mx_scale_fmt sfmt, mx_layout layout,
+                      void* q_row, void* s_row, void* q_col, void* s_col, void* stream);
+
+/*
+ * mx_gemm -- MXFP8 block-scaled GEMM.  [MX] sec 0.3:
+ *   C[m][n] = sum_b sA[m][b] sB[n][b] sum_{i<32} qA[m][32b+i] qB[n][32b+i], FP32 accumulate.
+ *
+ * qa[M][K], qb[N][K]: E4M3 or E5M2 codes (ea, eb), 16-byte aligned; sa, sb: E8M0 scales in
+ * the MX GEMM layout.  out: M rows of ldc elements (ldc >= N, ldc % 8 == 0), FP32 or bf16
+ * (RNE).  M % 128 == 0, N % 128 == 0, K % 128 == 0.
+ */
+mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea,
+                  const void* qb, const void* sb, mx_elem eb,
+                  int64_t M, int64_t N, int64_t K,
+                  void* out, mx_out out_dtype, int64_t ldc, void* stream);
+
+/* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
+size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
+
+/*
+ * nvfp4_quantize -- NVFP4 two-level quantization.  [NV] sec 5.4, 5.6.
+ *   pass 1: amax over the whole tensor; s_g = fl32(amax / 2688) (1.0 if amax == 0),
+ *           written to *gscale (device float).
+ *   pass 2: per 16 consecutive elements along cols: t = fl32(fl32(bamax / 6) / s_g);
+ *           c = E4M3 RNE-satfinite(t); s_hat = fl32(dec(c) * s_g);
+ *           q = E2M1 RNE-satfinite(fl32(x / s_hat)) (0 when s_hat == 0).
+ * x[rows][cols] bf16 (finite); q_packed[rows][cols/2] u8; s_ue4m3: rows*cols/16 bytes in the
+ * NVFP4 GEMM layout; workspace: nvfp4_workspace_bytes() bytes, 16-byte aligned, contents
+ * need not be initialised (the call clears it on `stream`).  rows % 128 == 0,
+ * cols % 64 == 0.
+ */
+mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols,
+                         void* q_packed, void* s_ue4m3, float* gscale,
+                         void* workspace, void* stream);
+
+/*
+ * nvfp4_gemm -- NVFP4 block-scaled GEMM.  [NV] sec 7.3-7.4:
+ *   C[m][n] = gA * gB * sum_b sA[m][b] sB[n][b] sum_{i<16} qA qB, FP32 accumulate; the two
+ *   global scales (device floats written by nvfp4_quantize) are applied in the epilogue.
+ * qa[M][K/2], qb[N][K/2] packed E2M1; sa, sb in the NVFP4 GEMM layout.
+ * M % 128 == 0, N % 128 == 0, K % 256 == 0; out as for mx_gemm.
+ */
+mx_status nvfp4_gemm(const void* qa, const void* sa, const float* ga,
+                     const void* qb, const void* sb, const float* gb,
+                     int64_t M, int64_t N, int64_t K,
+                     void* out, mx_out out_dtype, int64_t ldc, void* stream);
+
+/*
+ * fp8_blockwise_gemm -- DeepSeek-style FP8 GEMM with FP32 promotion.  [DS] sec 6.3:
+ *   for every 128-wide k-block kb: P = sum_{k in kb} qA[m][k] qB[n][k] (tensor cores, FP32),
+ *   acc += sA[kb][m] * sB[n/128][kb] * P in FP32 registers.
+ * qa[M][K], qb[N][K] E4M3; sa float[K/128][M] (1x128 tiles, k-block-major);
+ * sb float[N/128][K/128] (128x128 blocks).  M % 128 == 0, N % 128 == 0, K % 128 == 0.
+ */
+mx_status fp8_blockwise_gemm(const void* qa, const float* sa,
+                             const void* qb, const float* sb,
+                             int64_t M, int64_t N, int64_t K,
+                             void* out, mx_out out_dtype, int64_t ldc, void* stream);
+
+/* Bytes of the scale tensor mx_quantize / nvfp4_quantize write for a [rows][cols] input:
+ * block 32 + E8M0 -> rows*cols/32; block 16 + UE4M3 -> rows*cols/16; block 128 + FP32 ->
+ * 4*rows*cols/128 (block_rows 1) or 4*(rows/128)*(cols/128) (block_rows 128).  0 if the
+ * combination is not supported. */
+size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_scale_fmt sfmt);
+
+/*
+ * mx_check -- synchronizes `stream`, then reads and clears the library's device error word.
+ * Returns MX_ERR_TIMEOUT if a kernel's bounded wait ran out since the last check,
+ * MX_ERR_CUDA on a pending CUDA error, MX_OK otherwise.  This is the only call that
+ * synchronizes.
+ */
+mx_status mx_check(void* stream);
+
+/* Number of SMs the GEMM kernels size their persistent grids for (0 before the first call
+ * that launches a GEMM on the current device). */
+int mx_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXGB_MX_H_ */

@@ -1,0 +1,110 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports every symbol that
+include/mx.h declares, and rejects invalid arguments on the host before any launch.  Also
+checks the test-side layout permutations."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_scaled_precision_mx_gb300 as mx
+from block_scaled_precision_mx_gb300 import build as mxbuild
+from tests.layouts import chunked_to_plain, plain_to_chunked, unpack_fp4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mxbuild.build()
+    return mx.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mx_quantize" in names and "fp8_blockwise_gemm" in names and "nvfp4_gemm" in names
+    cdll = ctypes.CDLL(mx.library_path())
+    for n in names:
+        assert hasattr(cdll, n), n
+    assert set(names) <= set(mx.EXPORTS)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.mx_abi_version() == 1
+    assert mx.status_string(mx.MX_OK) == "MX_OK"
+    assert mx.status_string(mx.MX_ERR_TIMEOUT) == "MX_ERR_TIMEOUT"
+    assert mx.status_string(99) == "MX_ERR_UNKNOWN"
+
+
+def test_scale_bytes(lib):
+    assert mx.mx_scale_bytes(16384, 4096, 32, 1, mx.SCALE_E8M0) == 16384 * 128
+    assert mx.mx_scale_bytes(8192, 8192, 16, 1, mx.SCALE_UE4M3) == 8192 * 512
+    assert mx.mx_scale_bytes(4096, 7168, 128, 1, mx.SCALE_FP32) == 4 * 4096 * 56
+    assert mx.mx_scale_bytes(2048, 7168, 128, 128, mx.SCALE_FP32) == 4 * 16 * 56
+    assert mx.mx_scale_bytes(128, 128, 64, 1, mx.SCALE_E8M0) == 0
+
+
+FAKE = 1 << 20  # non-null, 16-byte aligned, never dereferenced: validation fails first
+
+
+def test_quantize_rejects_bad_arguments(lib):
+    q = lib.mx_quantize
+    ok_args = dict(x=FAKE, rows=256, cols=256, block=32, block_rows=1, elem=0, sfmt=0, layout=3,
+                   qr=FAKE, sr=FAKE, qc=FAKE, sc=FAKE)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return q(a["x"], a["rows"], a["cols"], a["block"], a["block_rows"], a["elem"], a["sfmt"], a["layout"],
+                 a["qr"], a["sr"], a["qc"], a["sc"], None)
+
+    assert call(x=None) == mx.MX_ERR_INVALID_ARG
+    assert call(rows=100) == mx.MX_ERR_INVALID_ARG
+    assert call(cols=0) == mx.MX_ERR_INVALID_ARG
+    assert call(x=FAKE + 8) == mx.MX_ERR_INVALID_ARG
+    assert call(elem=7) == mx.MX_ERR_INVALID_ARG
+    assert call(layout=0) == mx.MX_ERR_INVALID_ARG
+    assert call(qc=None) == mx.MX_ERR_INVALID_ARG          # column-wise requested, no buffer
+    assert call(block=64) == mx.MX_ERR_UNSUPPORTED
+    assert call(block=128, sfmt=2, layout=2) == mx.MX_ERR_UNSUPPORTED   # DeepSeek column-wise
+    assert call(elem=2) == mx.MX_ERR_UNSUPPORTED            # E2M1 with E8M0 (MXFP4) not built
+
+
+def test_gemms_reject_bad_arguments(lib):
+    g = lib.mx_gemm
+    assert g(None, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 100, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 96, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 64, None) == mx.MX_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 5, 128, None) == mx.MX_ERR_INVALID_ARG
+    assert g(FAKE, FAKE, 2, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_UNSUPPORTED
+    n = lib.nvfp4_gemm
+    assert n(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 128, FAKE, 0, 128, None) == mx.MX_ERR_INVALID_ARG
+    assert n(FAKE, FAKE, None, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 0, 128, None) == mx.MX_ERR_INVALID_ARG
+    d = lib.fp8_blockwise_gemm
+    assert d(FAKE, FAKE, FAKE, FAKE, 128, 100, 128, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG
+    nq = lib.nvfp4_quantize
+    assert nq(FAKE, 128, 96, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert nq(FAKE, 128, 128, FAKE, FAKE, FAKE, None, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.nvfp4_workspace_bytes(8192, 8192) >= 16
+
+
+def test_layout_permutations_roundtrip():
+    rng = np.random.default_rng(0)
+    plain = rng.integers(0, 256, (256, 12), dtype=np.uint8)
+    flat = plain_to_chunked(plain)
+    assert flat.shape == (256 * 12,)
+    assert np.array_equal(chunked_to_plain(flat, 256, 12), plain)
+    # spot-check the documented byte offset: row 128*rb + i, block 4*kc + j
+    rb, i, kc, j = 1, 77, 2, 3
+    off = (rb * 3 + kc) * 512 + (i % 32) * 16 + (i // 32) * 4 + j
+    assert flat[off] == plain[128 * rb + i, 4 * kc + j]
+    qp = np.array([[0x21, 0x43]], np.uint8)
+    assert unpack_fp4(qp).tolist() == [[1, 2, 3, 4]]
