@@ -316,7 +316,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -399,26 +399,36 @@ def main():
     rows_ms = {n: v / args.steps for n, v in rows_ms.items()}
     rows = {n: row_report(n, rows_ms[n], peaks) for n in ROW_ORDER}
 
-    # dominant kernel: the largest share of the step
-    dom = max(ROW_ORDER, key=lambda n: rows_ms[n])
-    launches_in_row = {"q2": 2, "linq": 3, "fprop": 1, "dgrad": 1, "wgrad": 1, "nvq": 4, "nvgemm": 1, "dsq": 2,
-                       "dsgemm": 1}
-    rep = rows[dom]
+    # dominant kernel: the kernel (all its launches in the step) with the largest share
+    kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
+               "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"]}
+    launches = {"mx_gemm": 3, "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1, "mx_quantize": 5, "nvfp4_quantize": 4,
+                "ds_quantize": 2}
+    dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
+    dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
-    if rep["bound"] == "tensor":
-        roof = {"bound": "tensor", "kernel": dom, "achieved": rep["TFLOP/s"], "unit": "TFLOP/s",
-                "peak": round(rep["TFLOP/s"] / rep["frac"], 1) if rep["frac"] else None,
-                "frac": rep["frac"], "traffic": traffic,
-                "peak_source": f"{peaks['source']}: bf16 sustained x {'4 (FP4)' if dom == 'nvgemm' else '2 (FP8)'}"
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm"):
+        flops = {"mx_gemm": 3 * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS}[dom]
+        peak = 2 * fp8_peak if dom == "nvfp4_gemm" else fp8_peak
+        ach = flops / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
+                "per_launch": {"flops": flops // launches[dom], "avg_ms": round(dom_ms / launches[dom], 4)},
+                "peak_source": f"{peaks['source']}: bf16 sustained x {'4 (FP4)' if dom == 'nvfp4_gemm' else '2 (FP8)'}"
                                " nominal dense ratio"}
     else:
-        roof = {"bound": "hbm", "kernel": dom, "achieved": rep["GB/s"], "unit": "GB/s", "peak": peaks["hbm_gbs"],
-                "frac": rep["frac"], "traffic": traffic, "peak_source": f"{peaks['source']} copy bandwidth"}
-    roof["launches_per_step"] = launches_in_row[dom]
+        b = {"mx_quantize": Q2_BYTES + LINQ_BYTES, "nvfp4_quantize": NVQ_BYTES, "ds_quantize": DSQ_BYTES}[dom]
+        ach = b / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "per_launch": {"bytes": int(b // launches[dom]), "avg_ms": round(dom_ms / launches[dom], 4)},
+                "peak_source": f"{peaks['source']} copy bandwidth"}
+    roof["launches_per_step"] = launches[dom]
 
     # end to end through the public API with host buffers
     e2e = None
