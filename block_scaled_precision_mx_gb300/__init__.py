@@ -30,6 +30,7 @@ OUT_F32, OUT_BF16 = 0, 1
 EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
+    "nvfp4_quantize_noalloc",
 )
 
 
@@ -70,6 +71,7 @@ def load():
             "mx_scale_bytes": (ctypes.c_size_t, [i64, i64, i32, i32, i32]),
             "mx_check": (i32, [vp]),
             "mx_num_sms": (i32, []),
+            "nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

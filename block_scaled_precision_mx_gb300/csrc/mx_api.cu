@@ -314,3 +314,103 @@ mx_status mx_check(void* stream) {
 }
 
 }  // extern "C"
+
+// =============================================================================================
+// nvfp4_quantize_noalloc: the NVFP4 quantizer for callers that cannot allocate device memory.
+//
+// nvfp4_quantize needs a small caller-provided workspace for the global amax.  Some callers have
+// no way to provide one: a plug-in running inside a host process whose allocator owns all of the
+// device memory, or a runtime that must never call cudaMalloc on its launch path because that
+// call synchronizes the whole device.  This variant keeps its scratch in the file-scope array
+// below, which the library reserves on every GPU it is loaded on, for as long as the process
+// lives.  The array holds one partial maximum per band of 16 input rows (16384 bands, 64 KB),
+// so inputs may have at most 262144 rows; larger inputs are rejected with MX_ERR_INVALID_ARG.
+// =============================================================================================
+namespace {
+constexpr int64_t kNoAllocBandRows = 16;
+constexpr int64_t kNoAllocSlots = 16384;
+constexpr int64_t kNoAllocMaxRows = kNoAllocBandRows * kNoAllocSlots;
+}  // namespace
+
+// slots [0, kNoAllocSlots): per-band partial maxima (FP32 bits); slot kNoAllocSlots: global amax
+static __device__ __align__(256) unsigned int g_nvfp4_noalloc_scratch[kNoAllocSlots + 64];
+
+namespace mxgb {
+
+// One CTA per band of 16 rows: the band's max |x| as FP32 bits.  Writes every slot it owns, so
+// nothing in the array has to be cleared between calls.
+__global__ void __launch_bounds__(256) nvfp4_band_amax_kernel(const uint16_t* __restrict__ x, int64_t cols,
+                                                              unsigned int* __restrict__ partial) {
+  __shared__ uint32_t wmax[8];
+  const uint16_t* xb = x + static_cast<int64_t>(blockIdx.x) * kNoAllocBandRows * cols;
+  const int64_t nvec = kNoAllocBandRows * cols / 8;
+  uint32_t m = 0;
+  for (int64_t i = threadIdx.x; i < nvec; i += 256) m = max(m, absmax_bits8(ld_stream_v4(xb + i * 8)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
+    partial[blockIdx.x] = m << 16;  // bf16 bits -> FP32 bits
+  }
+}
+
+// One CTA: maximum over the first `nbands` partial maxima -> *amax_out.
+__global__ void __launch_bounds__(1024) nvfp4_amax_finalize_kernel(const unsigned int* __restrict__ partial,
+                                                                   int64_t nbands, unsigned int* __restrict__ amax_out) {
+  __shared__ uint32_t wmax[32];
+  uint32_t m = 0;
+  for (int64_t i = threadIdx.x; i < nbands; i += 1024) m = max(m, partial[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < 32; ++i) m = max(m, wmax[i]);
+    *amax_out = m;
+  }
+}
+
+}  // namespace mxgb
+
+namespace {
+// Device address of the scratch array, looked up once per device with that device current.
+unsigned int* noalloc_scratch() {
+  static std::mutex mu;
+  static unsigned int* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_nvfp4_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    addr[dev] = static_cast<unsigned int*>(p);
+  }
+  return addr[dev];
+}
+}  // namespace
+
+extern "C" mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, void* q_packed,
+                                            void* s_ue4m3, float* gscale, void* stream) {
+  if (!x || !q_packed || !s_ue4m3 || !gscale) return MX_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0 || rows % 128 || cols % 64) return MX_ERR_INVALID_ARG;
+  if (rows > kNoAllocMaxRows || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q_packed, 16) || !aligned(s_ue4m3, 16) || !aligned(gscale, 4))
+    return MX_ERR_INVALID_ARG;
+  unsigned int* scratch = noalloc_scratch();
+  if (!scratch) return MX_ERR_CUDA;
+  cudaStream_t st = as_stream(stream);
+  const int64_t nbands = rows / kNoAllocBandRows;
+  nvfp4_band_amax_kernel<<<static_cast<unsigned>(nbands), 256, 0, st>>>(static_cast<const uint16_t*>(x), cols,
+                                                                         scratch);
+  if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
+  nvfp4_amax_finalize_kernel<<<1, 1024, 0, st>>>(scratch, nbands, scratch + kNoAllocSlots);
+  if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
+  const int64_t ctas = (rows / 32) * ((cols + 127) / 128);
+  if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(
+      static_cast<const uint16_t*>(x), rows, cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3),
+      gscale, scratch + kNoAllocSlots);
+  return launch_status();
+}

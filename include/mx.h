@@ -157,6 +157,25 @@ mx_status fp8_blockwise_gemm(const void* qa, const float* sa,
                              int64_t M, int64_t N, int64_t K,
                              void* out, mx_out out_dtype, int64_t ldc, void* stream);
 
+/*
+ * nvfp4_quantize_noalloc -- the same NVFP4 quantization as nvfp4_quantize, for callers that
+ * cannot allocate device memory (for example a plug-in inside a host whose allocator owns all of
+ * the GPU's memory, or a launch path that must never call cudaMalloc because it synchronizes the
+ * device).  It takes no workspace and allocates nothing: its scratch is a 64 KB array inside
+ * libmxgb.so that every GPU which loads the library keeps until the process exits.  The pages
+ * have no counterpart to this entry point; it exists only for such callers.
+ *
+ * Arguments and results are those of nvfp4_quantize (identical codes, scales and gscale).
+ * Limit: rows <= 262144 (the array holds one partial maximum per 16 rows); larger inputs return
+ * MX_ERR_INVALID_ARG.  The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.  All calls share the one
+ * array: calls that overlap on the GPU (different streams, or different host threads, without
+ * ordering between them) race and may produce wrong results.  Each call writes every scratch slot
+ * it reads before reading it, so nothing left by an earlier call needs clearing.
+ */
+mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols,
+                                 void* q_packed, void* s_ue4m3, float* gscale, void* stream);
+
 /* Bytes of the scale tensor mx_quantize / nvfp4_quantize write for a [rows][cols] input:
  * block 32 + E8M0 -> rows*cols/32; block 16 + UE4M3 -> rows*cols/16; block 128 + FP32 ->
  * 4*rows*cols/128 (block_rows 1) or 4*(rows/128)*(cols/128) (block_rows 128).  0 if the
