@@ -134,73 +134,99 @@ class ClockSampler:
 class Workload:
     """All inputs and outputs of one step, resident on the device."""
 
-    def __init__(self, dev):
+    GROUPS = ("q2", "lin", "nv", "ds")
+
+    def __init__(self, dev, groups=GROUPS):
         import torch
         from block_scaled_precision_mx_gb300 import synthetic
         import block_scaled_precision_mx_gb300 as mx
         self.mx = mx
         self.torch = torch
         self.dev = dev
+        self.groups = tuple(groups)
         t = lambda x: x.to(dev)
         self.host = {}
-        self.host["x2"] = synthetic.mxfp8_quantize()
-        self.host["X"], self.host["W"], self.host["G"] = synthetic.mxfp8_linear()
-        self.host["A4"], self.host["B4"] = synthetic.nvfp4_pair()
-        self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
+        if "q2" in groups:
+            self.host["x2"] = synthetic.mxfp8_quantize()
+        if "lin" in groups:
+            self.host["X"], self.host["W"], self.host["G"] = synthetic.mxfp8_linear()
+        if "nv" in groups:
+            self.host["A4"], self.host["B4"] = synthetic.nvfp4_pair()
+        if "ds" in groups:
+            self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
         self.d = {k: t(v) for k, v in self.host.items()}
         u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
         f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)
         bf = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
         sb = mx.mx_scale_bytes
-        # q2 outputs (E4M3 and E5M2)
-        self.q2 = {e: (u8(16384, 4096), u8(sb(16384, 4096)), u8(4096, 16384), u8(sb(4096, 16384))) for e in (0, 1)}
-        self.Xq = (u8(8192, 4096), u8(sb(8192, 4096)), u8(4096, 8192), u8(sb(4096, 8192)))
-        self.Wq = (u8(14336, 4096), u8(sb(14336, 4096)), u8(4096, 14336), u8(sb(4096, 14336)))
-        self.Gq = (u8(8192, 14336), u8(sb(8192, 14336)), u8(14336, 8192), u8(sb(14336, 8192)))
-        self.Y, self.dX, self.dW = bf(8192, 14336), bf(8192, 4096), bf(14336, 4096)
-        self.A4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
-        self.B4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
-        self.Y4 = f32(8192, 8192)
-        self.A5q = (u8(4096, 7168), f32(56, 4096))
-        self.B5q = (u8(2048, 7168), f32(16, 56))
-        self.Y5 = bf(4096, 2048)
-        self.launches_per_step = 2 + 6 + 5 + 3
+        self.launches_per_step = 0
+        self._outs = []
+        if "q2" in groups:   # E4M3 and E5M2 outputs
+            self.q2 = {e: (u8(16384, 4096), u8(sb(16384, 4096)), u8(4096, 16384), u8(sb(4096, 16384))) for e in (0, 1)}
+            self.launches_per_step += 2
+            self._outs += [self.q2[0][0], self.q2[0][2], self.q2[1][0], self.q2[1][2]]
+        if "lin" in groups:
+            self.Xq = (u8(8192, 4096), u8(sb(8192, 4096)), u8(4096, 8192), u8(sb(4096, 8192)))
+            self.Wq = (u8(14336, 4096), u8(sb(14336, 4096)), u8(4096, 14336), u8(sb(4096, 14336)))
+            self.Gq = (u8(8192, 14336), u8(sb(8192, 14336)), u8(14336, 8192), u8(sb(14336, 8192)))
+            self.Y, self.dX, self.dW = bf(8192, 14336), bf(8192, 4096), bf(14336, 4096)
+            self.launches_per_step += 6
+            self._outs += [self.Y, self.dX, self.dW]
+        if "nv" in groups:
+            self.A4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
+            self.B4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
+            self.Y4 = f32(8192, 8192)
+            self.launches_per_step += 5
+            self._outs += [self.Y4]
+        if "ds" in groups:
+            self.A5q = (u8(4096, 7168), f32(56, 4096))
+            self.B5q = (u8(2048, 7168), f32(16, 56))
+            self.Y5 = bf(4096, 2048)
+            self.launches_per_step += 3
+            self._outs += [self.Y5]
 
     def outputs(self):
-        return [self.q2[0][0], self.q2[0][2], self.q2[1][0], self.q2[1][2], self.Y, self.dX, self.dW, self.Y4, self.Y5]
+        return list(self._outs)
 
     def step(self, ev=None):
         """One pass of the hot path.  `ev(name)` records a CUDA event at row boundaries."""
         mx = self.mx
         d = self.d
         mark = ev or (lambda name: None)
-        mark("q2")
-        for e in (0, 1):
-            q = self.q2[e]
-            mx.mx_quantize(d["x2"], elem=e, layout=mx.BOTH, q_row=q[0], s_row=q[1], q_col=q[2], s_col=q[3])
-        mark("linq")
-        for src, dst, e in ((d["X"], self.Xq, 0), (d["W"], self.Wq, 0), (d["G"], self.Gq, 1)):
-            mx.mx_quantize(src, elem=e, layout=mx.BOTH, q_row=dst[0], s_row=dst[1], q_col=dst[2], s_col=dst[3])
-        mark("fprop")
-        mx.mx_gemm(self.Xq[0], self.Xq[1], 0, self.Wq[0], self.Wq[1], 0, 8192, 14336, 4096, mx.OUT_BF16, out=self.Y)
-        mark("dgrad")
-        mx.mx_gemm(self.Gq[0], self.Gq[1], 1, self.Wq[2], self.Wq[3], 0, 8192, 4096, 14336, mx.OUT_BF16, out=self.dX)
-        mark("wgrad")
-        mx.mx_gemm(self.Gq[2], self.Gq[3], 1, self.Xq[2], self.Xq[3], 0, 14336, 4096, 8192, mx.OUT_BF16, out=self.dW)
-        mark("nvq")
-        for src, dst in ((d["A4"], self.A4q), (d["B4"], self.B4q)):
-            mx.nvfp4_quantize(src, q_packed=dst[0], s_ue4m3=dst[1], gscale=dst[2], workspace=dst[3])
-        mark("nvgemm")
-        mx.nvfp4_gemm(self.A4q[0], self.A4q[1], self.A4q[2], self.B4q[0], self.B4q[1], self.B4q[2], 8192, 8192,
-                      8192, mx.OUT_F32, out=self.Y4)
-        mark("dsq")
-        mx.mx_quantize(d["A5"], block=128, block_rows=1, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
-                       q_row=self.A5q[0], s_row=self.A5q[1])
-        mx.mx_quantize(d["B5"], block=128, block_rows=128, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
-                       q_row=self.B5q[0], s_row=self.B5q[1])
-        mark("dsgemm")
-        mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
-                              out=self.Y5)
+        g = self.groups
+        if "q2" in g:
+            mark("q2")
+            for e in (0, 1):
+                q = self.q2[e]
+                mx.mx_quantize(d["x2"], elem=e, layout=mx.BOTH, q_row=q[0], s_row=q[1], q_col=q[2], s_col=q[3])
+        if "lin" in g:
+            mark("linq")
+            for src, dst, e in ((d["X"], self.Xq, 0), (d["W"], self.Wq, 0), (d["G"], self.Gq, 1)):
+                mx.mx_quantize(src, elem=e, layout=mx.BOTH, q_row=dst[0], s_row=dst[1], q_col=dst[2], s_col=dst[3])
+            mark("fprop")
+            mx.mx_gemm(self.Xq[0], self.Xq[1], 0, self.Wq[0], self.Wq[1], 0, 8192, 14336, 4096, mx.OUT_BF16, out=self.Y)
+            mark("dgrad")
+            mx.mx_gemm(self.Gq[0], self.Gq[1], 1, self.Wq[2], self.Wq[3], 0, 8192, 4096, 14336, mx.OUT_BF16,
+                       out=self.dX)
+            mark("wgrad")
+            mx.mx_gemm(self.Gq[2], self.Gq[3], 1, self.Xq[2], self.Xq[3], 0, 14336, 4096, 8192, mx.OUT_BF16,
+                       out=self.dW)
+        if "nv" in g:
+            mark("nvq")
+            for src, dst in ((d["A4"], self.A4q), (d["B4"], self.B4q)):
+                mx.nvfp4_quantize(src, q_packed=dst[0], s_ue4m3=dst[1], gscale=dst[2], workspace=dst[3])
+            mark("nvgemm")
+            mx.nvfp4_gemm(self.A4q[0], self.A4q[1], self.A4q[2], self.B4q[0], self.B4q[1], self.B4q[2], 8192, 8192,
+                          8192, mx.OUT_F32, out=self.Y4)
+        if "ds" in g:
+            mark("dsq")
+            mx.mx_quantize(d["A5"], block=128, block_rows=1, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                           q_row=self.A5q[0], s_row=self.A5q[1])
+            mx.mx_quantize(d["B5"], block=128, block_rows=128, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                           q_row=self.B5q[0], s_row=self.B5q[1])
+            mark("dsgemm")
+            mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
+                                  out=self.Y5)
         mark("end")
 
 
@@ -210,8 +236,8 @@ ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "d
 def row_report(name, ms, peaks):
     """Per-row throughput and roofline fraction from its average time per step (ms)."""
     s = ms / 1e3
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (nominal ratio)
-    fp4_peak = 4.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 4x BF16 (nominal ratio)
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (4.5 / 2.25 nominal)
+    fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
     if name in ("q2", "linq", "nvq", "dsq"):
         b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES}[name]
         gbs = b / s / 1e9
@@ -284,6 +310,21 @@ def oracle_sample_run():
 
 
 # ------------------------------------------------------------------------------------ main
+def max_over_ranks(ms, dist=None, device=None):
+    """Slowest rank's time (ms): the whole job finishes when the last replica does."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_max):
+    """Whole-job throughput: units every rank processed / the slowest rank's time (per second)."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -321,6 +362,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--only", default=None,
+                    help="comma-separated subset of row groups (q2, lin, nv, ds) for profiling runs; "
+                         "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -345,7 +389,8 @@ def main():
         pg = dist
     peaks = load_peaks()
 
-    wl = Workload(dev)
+    groups = tuple(args.only.split(",")) if args.only else Workload.GROUPS
+    wl = Workload(dev, groups)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wl.step()
@@ -385,11 +430,7 @@ def main():
     status = mx.mx_check()
     if status != mx.MX_OK:
         raise RuntimeError(f"device status after timed region: {mx.status_string(status)}")
-    ms_total = start.elapsed_time(stop)
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(start.elapsed_time(stop), pg, dev)
     ms_step = ms_total / args.steps
 
     rows_ms = {n: 0.0 for n in ROW_ORDER}
@@ -397,13 +438,17 @@ def main():
         for (n, e0), (_, e1) in zip(lst[:-1], lst[1:]):
             rows_ms[n] += e0.elapsed_time(e1)
     rows_ms = {n: v / args.steps for n, v in rows_ms.items()}
-    rows = {n: row_report(n, rows_ms[n], peaks) for n in ROW_ORDER}
+    present = [n for n in ROW_ORDER if rows_ms[n] > 0]
+    rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
+    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS}
+    step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
     kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
                "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"]}
     launches = {"mx_gemm": 3, "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1, "mx_quantize": 5, "nvfp4_quantize": 4,
                 "ds_quantize": 2}
+    kernels = {k: v for k, v in kernels.items() if all(r in present for r in v)}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -414,12 +459,12 @@ def main():
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm"):
         flops = {"mx_gemm": 3 * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS}[dom]
-        peak = 2 * fp8_peak if dom == "nvfp4_gemm" else fp8_peak
+        peak = 3 * fp8_peak if dom == "nvfp4_gemm" else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
                 "per_launch": {"flops": flops // launches[dom], "avg_ms": round(dom_ms / launches[dom], 4)},
-                "peak_source": f"{peaks['source']}: bf16 sustained x {'4 (FP4)' if dom == 'nvfp4_gemm' else '2 (FP8)'}"
+                "peak_source": f"{peaks['source']}: bf16 sustained x {'6 (FP4)' if dom == 'nvfp4_gemm' else '2 (FP8)'}"
                                " nominal dense ratio"}
     else:
         b = {"mx_quantize": Q2_BYTES + LINQ_BYTES, "nvfp4_quantize": NVQ_BYTES, "ds_quantize": DSQ_BYTES}[dom]
@@ -454,24 +499,21 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if pg:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * GEMM_FLOPS_STEP / (e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, pg, dev)
+        e2e = {"value": round(job_throughput(step_flops, world, e_ms) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     clocks = sampler.summary(t_wall0, t_wall1)
-    value = world * GEMM_FLOPS_STEP / (ms_step / 1e3) / 1e12
+    value = job_throughput(step_flops, world, ms_step) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8/fp4 inputs, f32 accumulate", "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (129 MB) between reuses; no explicit flush",
-                   "quantize_GB/s": round((Q2_BYTES + LINQ_BYTES + NVQ_BYTES + DSQ_BYTES) /
-                                          (sum(rows_ms[n] for n in ('q2', 'linq', 'nvq', 'dsq')) / 1e3) / 1e9, 1)},
+                   "quantize_GB/s": round(sum(rows[n]["bytes"] for n in present if "bytes" in rows[n]) /
+                                          (sum(rows_ms[n] for n in present if "bytes" in rows[n]) / 1e3) / 1e9, 1)
+                   if any("bytes" in rows[n] for n in present) else None},
         "rows": rows,
         "roofline": roof,
         "gpu_launches": wl.launches_per_step * args.steps,
@@ -483,6 +525,9 @@ def main():
         line["cpu_baseline"] = {"value": round(GEMM_FLOPS_STEP / t_cpu / 1e12, 6), "unit": "TFLOP/s",
                                 "cores": threads, "kind": "oracle", "sample": desc,
                                 "projected_step_s": round(t_cpu, 2)}
+    if args.only:
+        line["config"]["only"] = args.only
+        line["note"] = "profiling subset (--only): not a bench value"
     if rank == 0:
         print(json.dumps(line))
     if pg:

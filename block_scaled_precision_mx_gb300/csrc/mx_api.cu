@@ -180,7 +180,7 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     if (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 4)) return MX_ERR_INVALID_ARG;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (block_rows == 1) {
-      const int64_t ctas = (rows / 32) * (cols / 128);
+      const int64_t ctas = (rows / 64) * (cols / 128);
       if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
       ds_quantize_1x128_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(xb, rows, cols,
                                                                             static_cast<uint8_t*>(q_row),

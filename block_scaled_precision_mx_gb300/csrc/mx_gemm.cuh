@@ -10,9 +10,9 @@
 //           "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 7.3 (four-step pipeline:
 //           narrow products, per-16 partial sums, times block scales, epilogue times the
 //           global scale) and sec 7.4 (scales of both operands).
-//   kDsF8 : DeepSeek FP8 -- kind::f8f6f4 over one 128-wide k-block at a time into one of two
+//   kDsF8 : DeepSeek FP8 -- kind::f8f6f4 over one 128-wide k-block at a time into one of four
 //           TMEM accumulators; epilogue warps promote every k-block into FP32 registers as
-//           acc += sA[kb][m] * sB[n/128][kb] * P while the tensor core fills the other buffer.
+//           acc += sA[kb][m] * sB[n/128][kb] * P while the tensor core fills the next buffers.
 //           "Why FP8 training is stable" (magicnetworld.com), sec 6.3 (N_C = 128 promotion,
 //           overlapped with MMA issue).
 //
@@ -21,7 +21,9 @@
 //               scale chunks (bulk copies) into a ring of smem stages.
 //   warp 1      TMEM allocation + single-thread MMA issue: tcgen05.cp of the stage's scale
 //               chunks into TMEM, then 4 tcgen05.mma (32 bytes of K each) per stage.
-//   warps 2..   epilogue: tcgen05.ld of the accumulator, scale / convert, vector stores.
+//   warps 2-9   epilogue, two warps per TMEM lane quarter: tcgen05.ld of the accumulator into
+//               registers, release of the accumulator, then scale / convert / vector stores
+//               (overlapping the next tile's MMAs).
 // Stages are handed over with mbarriers (TMA complete_tx -> MMA; tcgen05.commit -> producer;
 // tcgen05.commit -> epilogue; epilogue arrivals -> MMA).  Every wait is bounded.
 #pragma once
@@ -50,8 +52,10 @@ struct GemmCfg {
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
   static constexpr int NUM_MMA = KBYTES / 32;  // tcgen05.mma per stage (32 bytes of K each)
-  // TMEM columns
-  static constexpr int ACC_COLS = (KIND == kDsF8) ? 2 * BN : BN;
+  // TMEM accumulators: one 128 x BN buffer for the block-scaled kinds (the epilogue drains it
+  // into registers and releases it at once); four 128-column k-block buffers for DeepSeek.
+  static constexpr int NBUF = (KIND == kDsF8) ? 4 : 1;
+  static constexpr int ACC_COLS = NBUF * BN;
   static constexpr int SFA_COL = ACC_COLS;
   static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : (KIND == kNvf4 ? 16 : 0);
   static constexpr int SFB_COL = SFA_COL + SFA_COLS;
@@ -59,11 +63,12 @@ struct GemmCfg {
   static constexpr int USED_COLS = SFB_COL + SFB_COLS;
   static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
                                    : USED_COLS <= 256 ? 256 : 512;
-  static constexpr int NUM_EPI_WARPS = (KIND == kDsF8) ? 8 : 4;
+  static constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of BN
   static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
   static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
   static_assert(STAGES >= 2, "not enough shared memory for two stages");
   static_assert(USED_COLS <= 512, "TMEM overflow");
+  static_assert(KIND != kDsF8 || BN == 128, "the promotion epilogue holds 64 columns per thread");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "bad BN");
 };
 
@@ -126,10 +131,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + Cfg::STAGES;
-  uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;   // [2]
-  uint64_t* tempty_bar = bars + 2 * Cfg::STAGES + 2;  // [2]
-  uint64_t* drain_bar = bars + 2 * Cfg::STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::STAGES + 5);
+  uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;       // [NBUF]
+  uint64_t* tempty_bar = bars + 2 * Cfg::STAGES + 4;  // [NBUF]
+  uint64_t* drain_bar = bars + 2 * Cfg::STAGES + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::STAGES + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < Cfg::NBUF; ++b) {
       mbar_init(&tfull_bar[b], 1);
       mbar_init(&tempty_bar[b], Cfg::EPI_THREADS);
     }
@@ -230,8 +235,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
         for (int kt = 0; kt < num_kt; ++kt) {
           uint32_t d_tmem = tmem_base;
           if (KIND == kDsF8) {
-            const uint32_t b = acc_it & 1;
-            if (!mbar_wait(&tempty_bar[b], ((acc_it >> 1) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
+            const uint32_t b = acc_it % Cfg::NBUF;
+            if (!mbar_wait(&tempty_bar[b], ((acc_it / Cfg::NBUF) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) {
               ok = false;
               break;
             }
@@ -282,7 +287,7 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
           }
           umma_commit(&empty_bar[stage]);  // frees the smem stage once these MMAs are done
           if (KIND == kDsF8) {
-            umma_commit(&tfull_bar[acc_it & 1]);  // one k-block ready for promotion
+            umma_commit(&tfull_bar[acc_it % Cfg::NBUF]);  // one k-block ready for promotion
             ++acc_it;
           }
           if (++stage == Cfg::STAGES) {
@@ -301,11 +306,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which half of the BN columns this warp owns
     const int row_in_tile = q * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     uint32_t acc_it = 0;
     if (KIND != kDsF8) {
+      constexpr int HALF = BN / 2;
+      constexpr int NCH = HALF / 32;
       float gscale = 1.0f;
       if (KIND == kNvf4) gscale = __fmul_rn(*args.ga, *args.gb);
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -314,55 +322,72 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
         bool ok = mbar_wait(&tfull_bar[0], acc_it & 1, abort_flag, kSiteEpiTmemFull);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
-        const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + lane_addr + c * 32, r);
-          tmem_ld_wait();
-          float v[32];
+        // drain this warp's 32 rows x HALF columns into registers, then hand the accumulator
+        // back so the next tile's MMAs overlap the conversion and the stores below
+        uint32_t r[NCH][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[i]), gscale)
-                                                              : __uint_as_float(r[i]);
-          store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + c * 32, v);
-        }
+        for (int c = 0; c < NCH; ++c) tmem_ld_32x32b_x32(tmem_base + lane_addr + half * HALF + c * 32, r[c]);
+        tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&tempty_bar[0]);
         ++acc_it;
+        const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[c][i]), gscale) : __uint_as_float(r[c][i]);
+          store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * HALF + c * 32, v);
+        }
       }
     } else {
-      // DeepSeek promotion: this warp owns rows q*32.. and columns [half*64, half*64+64)
-      const int half = (warp - 2) >> 2;
+      // DeepSeek promotion: this warp owns rows q*32.. and columns [half*64, half*64+64).  The
+      // per-k-block scales are loaded two k-blocks ahead so their latency hides behind the MMAs.
       const int64_t kbs = args.K / 128;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, num_mb, num_nb, mb, nb);
         const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
+        const float* sa_row = args.dsa + row;
+        const float* sb_blk = args.dsb + static_cast<int64_t>(nb) * kbs;
+        float sa1 = __ldg(sa_row), sb1 = __ldg(sb_blk);
+        float sa2 = 0.0f, sb2 = 0.0f;
+        if (num_kt > 1) {
+          sa2 = __ldg(sa_row + args.M);
+          sb2 = __ldg(sb_blk + 1);
+        }
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
         for (int kt = 0; kt < num_kt; ++kt) {
-          const uint32_t b = acc_it & 1;
-          ok = mbar_wait(&tfull_bar[b], (acc_it >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+          const float sa_c = sa1, sb_c = sb1;
+          sa1 = sa2;
+          sb1 = sb2;
+          if (kt + 2 < num_kt) {
+            sa2 = __ldg(sa_row + static_cast<int64_t>(kt + 2) * args.M);
+            sb2 = __ldg(sb_blk + kt + 2);
+          }
+          const uint32_t b = acc_it % Cfg::NBUF;
+          ok = mbar_wait(&tfull_bar[b], (acc_it / Cfg::NBUF) & 1, abort_flag, kSiteEpiTmemFull);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float s = __fmul_rn(args.dsa[static_cast<int64_t>(kt) * args.M + row],
-                                    args.dsb[static_cast<int64_t>(nb) * (BN / 128) * kbs + kt]);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64 + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[i]), acc[c * 32 + i]);
-          }
+          uint32_t r[2][32];
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64, r[0]);
+          tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64 + 32, r[1]);
+          tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&tempty_bar[b]);
           ++acc_it;
+          const float s = __fmul_rn(sa_c, sb_c);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[c][i]), acc[c * 32 + i]);
         }
         if (!ok) break;
         store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64, acc);

@@ -84,6 +84,44 @@ __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
   return m;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Codes of fl32(x / d) without a per-element IEEE division.
+//
+// The recipes define the code as the rounding of the FP32 quotient fl32(x / d).  With
+// r = fl32(1 / d), the product x * r is within 1.5 FP32 ulp of fl32(x / d).  Converting
+// x * r * (1 - 2^-20) and x * r * (1 + 2^-20) brackets fl32(x / d); the conversions are monotonic,
+// so when both ends give the same code no rounding boundary of the format lies in between and
+// that code is the code of fl32(x / d).  When they differ (a boundary within ~2^-20 of the
+// quotient, rare) the IEEE quotient decides.  The result is therefore identical to converting
+// __fdiv_rn(x, d).  `d` must be a normal float no larger than 2^125 (callers check).
+// ---------------------------------------------------------------------------------------------
+struct QuotientBracket {
+  float lo, hi;  // fl32(1/d) scaled by (1 - 2^-20) and (1 + 2^-20)
+  float d;
+  __device__ __forceinline__ explicit QuotientBracket(float div) : d(div) {
+    const float r = __frcp_rn(div);
+    lo = __fmul_rn(r, 1.0f - 9.5367431640625e-07f);
+    hi = __fmul_rn(r, 1.0f + 9.5367431640625e-07f);
+  }
+  __device__ __forceinline__ static bool usable(float div) { return div >= 1.17549435e-38f && div <= 4.2535296e37f; }
+};
+
+// E4M3 pair (lo byte = a) of fl32(a / d), fl32(b / d)
+__device__ __forceinline__ uint32_t e4m3x2_quotient(float a, float b, const QuotientBracket& q) {
+  const uint32_t c0 = cvt_e4m3x2(__fmul_rn(a, q.lo), __fmul_rn(b, q.lo));
+  const uint32_t c1 = cvt_e4m3x2(__fmul_rn(a, q.hi), __fmul_rn(b, q.hi));
+  if (c0 == c1) return c0;
+  return cvt_e4m3x2(__fdiv_rn(a, q.d), __fdiv_rn(b, q.d));
+}
+
+// E2M1 pair (low nibble = a) of fl32(a / d), fl32(b / d)
+__device__ __forceinline__ uint32_t e2m1x2_quotient(float a, float b, const QuotientBracket& q) {
+  const uint32_t c0 = cvt_e2m1x2(__fmul_rn(a, q.lo), __fmul_rn(b, q.lo));
+  const uint32_t c1 = cvt_e2m1x2(__fmul_rn(a, q.hi), __fmul_rn(b, q.hi));
+  if (c0 == c1) return c0;
+  return cvt_e2m1x2(__fdiv_rn(a, q.d), __fdiv_rn(b, q.d));
+}
+
 template <int ELEM, bool ROW, bool COL>
 __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, uint8_t* __restrict__ q_row,
@@ -191,9 +229,9 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------------------------
-// DeepSeek 1x128: one warp per (row, 128-block); lane holds 4 consecutive bf16.
-// s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored [K/128][rows].
-// CTA = 8 warps = 8 consecutive rows of the same k-block, 4 iterations -> 32 rows.
+// DeepSeek 1x128: s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored
+// [K/128][rows].  CTA = 64 rows x one 128-column k-block; 16 lanes per row, 8 bf16 per lane
+// (one 128-bit load), the row maximum reduced over the 16 lanes of a half warp.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ q,
@@ -201,23 +239,36 @@ __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* 
   const int64_t kb_count = cols >> 7;
   const int64_t kb = blockIdx.x % kb_count;
   const int64_t rgrp = blockIdx.x / kb_count;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = threadIdx.x;
+  const int lc = t & 15;
+  uint4 v[4];
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int64_t r = rgrp * 32 + it * 8 + warp;
-    const uint2 v = *reinterpret_cast<const uint2*>(x + r * cols + kb * 128 + lane * 4);
-    const uint32_t w[2] = {v.x, v.y};
-    uint32_t m = max(max(w[0] & 0x7FFFu, (w[0] >> 16) & 0x7FFFu), max(w[1] & 0x7FFFu, (w[1] >> 16) & 0x7FFFu));
+  for (int i = 0; i < 4; ++i) {
+    const int64_t r = rgrp * 64 + (t >> 4) + 16 * i;
+    v[i] = ld_stream_v4(x + r * cols + kb * 128 + lc * 8);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    const float amax = bf16_bits_to_float(m);
-    const float sc = (m == 0) ? 1.0f : __fdiv_rn(amax, 448.0f);
-    const float f0 = __fdiv_rn(bf16_bits_to_float(w[0] & 0xFFFFu), sc);
-    const float f1 = __fdiv_rn(bf16_bits_to_float(w[0] >> 16), sc);
-    const float f2 = __fdiv_rn(bf16_bits_to_float(w[1] & 0xFFFFu), sc);
-    const float f3 = __fdiv_rn(bf16_bits_to_float(w[1] >> 16), sc);
-    *reinterpret_cast<uint32_t*>(q + r * cols + kb * 128 + lane * 4) = cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16);
-    if (lane == 0) s[kb * rows + r] = sc;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t r = rgrp * 64 + (t >> 4) + 16 * i;
+    uint32_t m = absmax_bits8(v[i]);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t p[4];
+    if (QuotientBracket::usable(sc)) {
+      const QuotientBracket qb(sc);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        p[j] = e4m3x2_quotient(bf16_bits_to_float(w[j] & 0xFFFFu), bf16_bits_to_float(w[j] >> 16), qb);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        p[j] = cvt_e4m3x2(__fdiv_rn(bf16_bits_to_float(w[j] & 0xFFFFu), sc),
+                          __fdiv_rn(bf16_bits_to_float(w[j] >> 16), sc));
+    }
+    *reinterpret_cast<uint2*>(q + r * cols + kb * 128 + lc * 8) = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+    if (lc == 0) s[kb * rows + r] = sc;
   }
 }
 
@@ -246,14 +297,17 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
   const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  const bool fast = QuotientBracket::usable(sc);
+  const QuotientBracket qb(fast ? sc : 1.0f);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t p[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      p[j] = cvt_e4m3x2(__fdiv_rn(bf16_bits_to_float(w[j] & 0xFFFFu), sc),
-                        __fdiv_rn(bf16_bits_to_float(w[j] >> 16), sc));
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_bits_to_float(w[j] & 0xFFFFu), b = bf16_bits_to_float(w[j] >> 16);
+      p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
+    }
     *reinterpret_cast<uint2*>(q + (br * 128 + r0 + 16 * i) * cols + bc * 128 + lc * 8) =
         make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
   }
@@ -315,11 +369,12 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   uint32_t lo = 0, hi = 0;
   if (s_hat != 0.0f) {
+    const bool fast = QuotientBracket::usable(s_hat);
+    const QuotientBracket qb(fast ? s_hat : 1.0f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float a = __fdiv_rn(bf16_bits_to_float(w[i] & 0xFFFFu), s_hat);
-      const float b = __fdiv_rn(bf16_bits_to_float(w[i] >> 16), s_hat);
-      const uint32_t byte = cvt_e2m1x2(a, b);
+      const float a = bf16_bits_to_float(w[i] & 0xFFFFu), b = bf16_bits_to_float(w[i] >> 16);
+      const uint32_t byte = fast ? e2m1x2_quotient(a, b, qb) : cvt_e2m1x2(__fdiv_rn(a, s_hat), __fdiv_rn(b, s_hat));
       if (i < 4) lo |= byte << (8 * i);
       else hi |= byte << (8 * (i - 4));
     }
