@@ -446,9 +446,11 @@ def main():
     # dominant kernel: the kernel (all its launches in the step) with the largest share
     kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
                "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"]}
-    launches = {"mx_gemm": 3, "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1, "mx_quantize": 5, "nvfp4_quantize": 4,
+    kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
+    kernels = {k: v for k, v in kernels.items() if v}
+    launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
+                "mx_quantize": 2 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2}
-    kernels = {k: v for k, v in kernels.items() if all(r in present for r in v)}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -458,7 +460,7 @@ def main():
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm"):
-        flops = {"mx_gemm": 3 * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS}[dom]
+        flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS}[dom]
         peak = 3 * fp8_peak if dom == "nvfp4_gemm" else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),
@@ -467,7 +469,7 @@ def main():
                 "peak_source": f"{peaks['source']}: bf16 sustained x {'6 (FP4)' if dom == 'nvfp4_gemm' else '2 (FP8)'}"
                                " nominal dense ratio"}
     else:
-        b = {"mx_quantize": Q2_BYTES + LINQ_BYTES, "nvfp4_quantize": NVQ_BYTES, "ds_quantize": DSQ_BYTES}[dom]
+        b = sum(rows[r]["bytes"] for r in kernels[dom])
         ach = b / (dom_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,

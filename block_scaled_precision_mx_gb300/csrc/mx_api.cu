@@ -12,6 +12,7 @@
 #include "../../include/mx.h"
 #include "mx_device.cuh"
 #include "mx_gemm.cuh"
+#include "mx_gemm2.cuh"
 #include "mx_quantize.cuh"
 
 using namespace mxgb;
@@ -44,8 +45,10 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor [rows][row_bytes], box 128 bytes x box_rows, 128-byte swizzle.
-bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+// 2-D byte tensor [rows][row_bytes], box 128 bytes x box_rows, 128-byte swizzle (swizzle=false:
+// unswizzled, used for scale chunks read as 128-byte rows).
+bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows,
+               bool swizzle = true) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
@@ -53,7 +56,7 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_byt
   cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -98,6 +101,48 @@ mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const Gemm
   const int tiles = (args.M / Cfg::BM) * (args.N / BN);
   const int grid = tiles < sms ? tiles : sms;
   kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, args);
+  return launch_status();
+}
+
+// CTA-pair kernel: clusters of two CTAs, each pair computing 256 x 256 output tiles.
+template <int KIND, bool OUT_BF16>
+mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
+  using Cfg = Gemm2Cfg<KIND>;
+  auto kern = bs_gemm2_kernel<KIND, OUT_BF16>;
+  static int max_clusters[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters[dev] == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+      return MX_ERR_CUDA;
+    const int sms = device_sms();
+    cfg.gridDim = dim3(static_cast<unsigned>(sms - (sms & 1)));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return MX_ERR_CUDA;
+    max_clusters[dev] = n;
+  }
+  const int64_t kc = (KIND == kMxf8) ? args.K / 128 : args.K / 64;
+  const int chunk_rows = Cfg::SF_CHUNK / 128;
+  CUtensorMap ta, tb, tsa, tsb;
+  if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
+  if (!make_tmap(&tb, qb, args.N, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
+  if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
+  if (!make_tmap(&tsb, args.sfb, (args.N / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
+  const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
+  const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, args) != cudaSuccess) return MX_ERR_CUDA;
   return launch_status();
 }
 
@@ -216,9 +261,13 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   const bool bn256 = (N % 256) == 0;
-  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 128, bn256 ? 256 : 128, 1);
   cudaStream_t st = as_stream(stream);
   const bool bf = out_dtype == MX_OUT_BF16;
+  if (bn256 && (M % 256) == 0) {
+    a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
+    return bf ? launch_gemm2<kMxf8, true>(qa, qb, K, a, st) : launch_gemm2<kMxf8, false>(qa, qb, K, a, st);
+  }
+  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 128, bn256 ? 256 : 128, 1);
   if (bn256) return bf ? launch_gemm<kMxf8, 256, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 256, false>(qa, qb, K, a, st);
   return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
 }
@@ -273,10 +322,14 @@ mx_status nvfp4_gemm(const void* qa, const void* sa, const float* ga, const void
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   const bool bn256 = (N % 256) == 0;
-  a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 0);
   cudaStream_t st = as_stream(stream);
   const bool bf = out_dtype == MX_OUT_BF16;
   const int64_t kb = K / 2;
+  if (bn256 && (M % 256) == 0) {
+    a.idesc = make_idesc_block_scaled(1u, 1u, 256, 256, 0);
+    return bf ? launch_gemm2<kNvf4, true>(qa, qb, kb, a, st) : launch_gemm2<kNvf4, false>(qa, qb, kb, a, st);
+  }
+  a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 0);
   if (bn256) return bf ? launch_gemm<kNvf4, 256, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 256, false>(qa, qb, kb, a, st);
   return bf ? launch_gemm<kNvf4, 128, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 128, false>(qa, qb, kb, a, st);
 }

@@ -56,11 +56,14 @@ struct GemmCfg {
   // into registers and releases it at once); four 128-column k-block buffers for DeepSeek.
   static constexpr int NBUF = (KIND == kDsF8) ? 4 : 1;
   static constexpr int ACC_COLS = NBUF * BN;
-  static constexpr int SFA_COL = ACC_COLS;
+  // Scale factors get their own TMEM columns per pipeline stage, so the tcgen05.cp of stage s+1
+  // carries no write-after-read dependency on the MMAs still reading stage s's scales.
   static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : (KIND == kNvf4 ? 16 : 0);
-  static constexpr int SFB_COL = SFA_COL + SFA_COLS;
   static constexpr int SFB_COLS = (KIND == kMxf8) ? 4 * RC : (KIND == kNvf4 ? 16 * RC : 0);
-  static constexpr int USED_COLS = SFB_COL + SFB_COLS;
+  static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
+  static constexpr int SFA_COL = ACC_COLS;             // + stage * SF_STAGE_COLS
+  static constexpr int SFB_COL = ACC_COLS + SFA_COLS;  // + stage * SF_STAGE_COLS
+  static constexpr int USED_COLS = ACC_COLS + STAGES * SF_STAGE_COLS;
   static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
                                    : USED_COLS <= 256 ? 256 : 512;
   static constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of BN
@@ -222,7 +225,15 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // The issue path of this single thread bounds the CTA's throughput, so per k-step it does only:
+    // the barrier waits, the scale copies (into the stage's own TMEM columns) and MMAs with
+    // descriptor words advanced by constants, and the commits.
     if (lane == 0) {
+      constexpr uint32_t kOpHi = smem_desc_hi(1024, kSwizzle128B);
+      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
+      constexpr uint32_t kLbo = smem_desc_lo_lbo(16);
+      const uint32_t a_lo0 = (smem_u32(sA) >> 4) | kLbo, b_lo0 = (smem_u32(sB) >> 4) | kLbo;
+      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_it = 0;  // accumulator hand-overs so far
@@ -248,39 +259,37 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * Cfg::A_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * Cfg::B_BYTES);
+          const uint32_t a_lo = a_lo0 + stage * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + stage * (Cfg::B_BYTES >> 4);
+          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
+          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
+          const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
+          const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
           if (KIND == kMxf8) {
-            tmem_cp_32x128b_warpx4(tmem_base + Cfg::SFA_COL,
-                                   make_smem_desc(smem_u32(sSFA + stage * Cfg::SFA_BYTES), 0, 128, kSwizzleNone));
+            tmem_cp_32x128b_warpx4(sfa_t, desc_from_words(sfa_lo, kSfHi));
 #pragma unroll
             for (int rc = 0; rc < Cfg::RC; ++rc)
-              tmem_cp_32x128b_warpx4(
-                  tmem_base + Cfg::SFB_COL + 4 * rc,
-                  make_smem_desc(smem_u32(sSFB + stage * Cfg::SFB_BYTES + rc * 512), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * rc, desc_from_words(sfb_lo + rc * (512 >> 4), kSfHi));
           } else if (KIND == kNvf4) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_warpx4(
-                  tmem_base + Cfg::SFA_COL + 4 * j,
-                  make_smem_desc(smem_u32(sSFA + stage * Cfg::SFA_BYTES + j * 512), 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
 #pragma unroll
               for (int rc = 0; rc < Cfg::RC; ++rc)
-                tmem_cp_32x128b_warpx4(tmem_base + Cfg::SFB_COL + j * 4 * Cfg::RC + 4 * rc,
-                                       make_smem_desc(smem_u32(sSFB + stage * Cfg::SFB_BYTES + rc * 2048 + j * 512),
-                                                      0, 128, kSwizzleNone));
+                tmem_cp_32x128b_warpx4(sfb_t + j * 4 * Cfg::RC + 4 * rc,
+                                       desc_from_words(sfb_lo + ((rc * 2048 + j * 512) >> 4), kSfHi));
             }
           }
 #pragma unroll
           for (int j = 0; j < Cfg::NUM_MMA; ++j) {
-            const uint64_t adesc = make_smem_desc(a_addr + j * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bdesc = make_smem_desc(b_addr + j * 32, 16, 1024, kSwizzle128B);
+            const uint64_t adesc = desc_from_words(a_lo + j * 2, kOpHi);  // + 32 bytes of K per MMA
+            const uint64_t bdesc = desc_from_words(b_lo + j * 2, kOpHi);
             if (KIND == kMxf8) {
-              umma_mxf8f6f4(d_tmem, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), tmem_base + Cfg::SFA_COL,
-                            tmem_base + Cfg::SFB_COL, (kt > 0 || j > 0) ? 1u : 0u);
+              umma_mxf8f6f4(d_tmem, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), sfa_t, sfb_t,
+                            (kt > 0 || j > 0) ? 1u : 0u);
             } else if (KIND == kNvf4) {
-              umma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, tmem_base + Cfg::SFA_COL + 4 * j,
-                            tmem_base + Cfg::SFB_COL + j * 4 * Cfg::RC, (kt > 0 || j > 0) ? 1u : 0u);
+              umma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * j, sfb_t + j * 4 * Cfg::RC,
+                            (kt > 0 || j > 0) ? 1u : 0u);
             } else {
               umma_f8f6f4(d_tmem, adesc, bdesc, args.idesc, j > 0 ? 1u : 0u);
             }
@@ -328,6 +337,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < NCH; ++c) tmem_ld_32x32b_x32(tmem_base + lane_addr + half * HALF + c * 32, r[c]);
         tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) tmem_regs_ready(r[c]);
         tc_fence_before();
         mbar_arrive(&tempty_bar[0]);
         ++acc_it;
@@ -342,8 +353,10 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
         }
       }
     } else {
-      // DeepSeek promotion: this warp owns rows q*32.. and columns [half*64, half*64+64).  The
-      // per-k-block scales are loaded two k-blocks ahead so their latency hides behind the MMAs.
+      // DeepSeek promotion: this warp owns rows q*32.. and columns [half*64, half*64+64).  K-blocks
+      // are promoted two at a time: both TMEM buffers are loaded before one wait, so one round trip
+      // (barrier wait, TMEM load, release) serves two k-blocks; each k-block still gets its own
+      // scale, in order.  The scales are loaded one pair ahead so their latency hides too.
       const int64_t kbs = args.K / 128;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -352,42 +365,63 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
         const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + row_in_tile;
         const float* sa_row = args.dsa + row;
         const float* sb_blk = args.dsb + static_cast<int64_t>(nb) * kbs;
-        float sa1 = __ldg(sa_row), sb1 = __ldg(sb_blk);
-        float sa2 = 0.0f, sb2 = 0.0f;
+        float nsa0 = __ldg(sa_row), nsb0 = __ldg(sb_blk);
+        float nsa1 = 0.0f, nsb1 = 0.0f;
         if (num_kt > 1) {
-          sa2 = __ldg(sa_row + args.M);
-          sb2 = __ldg(sb_blk + 1);
+          nsa1 = __ldg(sa_row + args.M);
+          nsb1 = __ldg(sb_blk + 1);
         }
         float acc[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-        for (int kt = 0; kt < num_kt; ++kt) {
-          const float sa_c = sa1, sb_c = sb1;
-          sa1 = sa2;
-          sb1 = sb2;
+        for (int kt = 0; kt < num_kt; kt += 2) {
+          const bool two = kt + 1 < num_kt;
+          const float s0 = __fmul_rn(nsa0, nsb0), s1 = __fmul_rn(nsa1, nsb1);
           if (kt + 2 < num_kt) {
-            sa2 = __ldg(sa_row + static_cast<int64_t>(kt + 2) * args.M);
-            sb2 = __ldg(sb_blk + kt + 2);
+            nsa0 = __ldg(sa_row + static_cast<int64_t>(kt + 2) * args.M);
+            nsb0 = __ldg(sb_blk + kt + 2);
           }
-          const uint32_t b = acc_it % Cfg::NBUF;
-          ok = mbar_wait(&tfull_bar[b], (acc_it / Cfg::NBUF) & 1, abort_flag, kSiteEpiTmemFull);
+          if (kt + 3 < num_kt) {
+            nsa1 = __ldg(sa_row + static_cast<int64_t>(kt + 3) * args.M);
+            nsb1 = __ldg(sb_blk + kt + 3);
+          }
+          const uint32_t b0 = acc_it % Cfg::NBUF, b1 = (acc_it + 1) % Cfg::NBUF;
+          ok = mbar_wait(&tfull_bar[b0], (acc_it / Cfg::NBUF) & 1, abort_flag, kSiteEpiTmemFull);
+          if (two) ok = ok && mbar_wait(&tfull_bar[b1], ((acc_it + 1) / Cfg::NBUF) & 1, abort_flag, kSiteEpiTmemFull);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint32_t r[2][32];
-          tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64, r[0]);
-          tmem_ld_32x32b_x32(tmem_base + lane_addr + b * BN + half * 64 + 32, r[1]);
+          uint32_t r0[32], r1[32];
+          const uint32_t t0 = tmem_base + lane_addr + b0 * BN + half * 64;
+          const uint32_t t1 = tmem_base + lane_addr + b1 * BN + half * 64;
+          tmem_ld_32x32b_x32(t0, r0);
+          tmem_ld_32x32b_x32(t0 + 32, r1);
           tmem_ld_wait();
+          tmem_regs_ready(r0);
+          tmem_regs_ready(r1);
           tc_fence_before();
-          mbar_arrive(&tempty_bar[b]);
-          ++acc_it;
-          const float s = __fmul_rn(sa_c, sb_c);
+          mbar_arrive(&tempty_bar[b0]);
+          // the second k-block's TMEM loads overlap the first one's FMAs
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(s0, __uint_as_float(r0[i]), acc[i]);
+          if (two) tmem_ld_32x32b_x32(t1, r0);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, __uint_as_float(r[c][i]), acc[c * 32 + i]);
+          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s0, __uint_as_float(r1[i]), acc[32 + i]);
+          if (two) {
+            tmem_ld_32x32b_x32(t1 + 32, r1);
+            tmem_ld_wait();
+            tmem_regs_ready(r0);
+            tmem_regs_ready(r1);
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[b1]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = fmaf(s1, __uint_as_float(r0[i]), acc[i]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s1, __uint_as_float(r1[i]), acc[32 + i]);
+          }
+          acc_it += two ? 2 : 1;
         }
         if (!ok) break;
         store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64, acc);

@@ -1,0 +1,276 @@
+// mx_gemm2.cuh -- block-scaled GEMMs on CTA pairs (tcgen05 cta_group::2) for sm_103a.
+//
+// Same products as the single-CTA kernel (kMxf8: MXFP8 with E8M0 scales per 32 of K; kNvf4:
+// NVFP4 with E4M3 scales per 16 and FP32 global scales in the epilogue), but one 256 x 256 output
+// tile is computed by a cluster of two CTAs on two SMs with M = 256 tcgen05.mma instructions:
+//   * each CTA loads its own 128 rows of A and its own 128 rows (half) of B per stage; the pair's
+//     MMA reads both halves of B, so every SM receives 2/3 of the operand bytes the single-CTA
+//     128 x 256 tile needs for the same number of MACs;
+//   * each CTA holds the scales of its 128 rows of A and the scales of all 256 rows of B; one
+//     pair-wide tcgen05.cp copies every CTA's scales from its own shared memory into its own TMEM,
+//     so the scale copies per MAC halve as well;
+//   * the leader CTA (rank 0) issues the MMAs and scale copies for the pair; both CTAs' TMA loads
+//     complete on the leader's stage barrier; the leader's commits arrive on the stage and
+//     accumulator barriers of both CTAs; both CTAs' epilogues drain their own TMEM accumulator
+//     (their 128 rows x 256 columns) and arrive on the leader's accumulator-free barrier.
+// Sources: "MXFP8 on SM120: software support" (xuesongtap.github.io), sec 0.3 (block-scaled
+// dot product); "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 7.3-7.4.
+#pragma once
+
+#include "mx_device.cuh"
+#include "mx_gemm.cuh"
+
+namespace mxgb {
+
+template <int KIND>
+struct Gemm2Cfg {
+  static constexpr int BM = 256;       // rows per pair tile (128 per CTA)
+  static constexpr int BN = 256;       // columns per pair tile
+  static constexpr int ROWS = 128;     // A rows and B rows each CTA loads
+  static constexpr int KBYTES = 128;   // bytes of K per stage
+  static constexpr int K_ELEMS = (KIND == kNvf4) ? 256 : 128;
+  static constexpr int A_BYTES = ROWS * KBYTES;
+  static constexpr int B_BYTES = ROWS * KBYTES;
+  static constexpr int SF_CHUNK = (KIND == kMxf8) ? 512 : 2048;  // scale bytes per 128 rows per stage
+  static constexpr int SFA_BYTES = SF_CHUNK;       // own 128 rows of A
+  static constexpr int SFB_BYTES = 2 * SF_CHUNK;   // all 256 rows of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int NUM_MMA = KBYTES / 32;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : 16;
+  static constexpr int SFB_COLS = (KIND == kMxf8) ? 8 : 32;
+  static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;  // each stage has its own scale columns
+  static constexpr int SFA_COL = ACC_COLS;                     // + stage * SF_STAGE_COLS
+  static constexpr int SFB_COL = ACC_COLS + SFA_COLS;          // + stage * SF_STAGE_COLS
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_EPI_WARPS = 8;
+  static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+  static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+  static_assert(STAGES >= 2, "not enough shared memory");
+  static_assert(ACC_COLS + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM overflow");
+};
+
+// Scale tensors are read through 2-D byte tensor maps with 128-byte rows (a 512-byte scale chunk
+// is 4 such rows), so that the peer CTA's scale loads can complete on the leader's barrier too.
+template <int KIND, bool OUT_BF16>
+__global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
+    bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                    const GemmArgs args) {
+  using Cfg = Gemm2Cfg<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + Cfg::STAGES * Cfg::A_BYTES;
+  uint8_t* sSFA = sB + Cfg::STAGES * Cfg::B_BYTES;
+  uint8_t* sSFB = sSFA + Cfg::STAGES * Cfg::SFA_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES);
+  uint64_t* full_bar = bars;                       // [STAGES], used in the leader
+  uint64_t* empty_bar = bars + Cfg::STAGES;        // [STAGES], both CTAs
+  uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;    // both CTAs
+  uint64_t* tempty_bar = tfull_bar + 1;            // used in the leader
+  uint64_t* drain_bar = tfull_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_bar + 3);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int num_mb = args.M / Cfg::BM;
+  const int num_nb = args.N / Cfg::BN;
+  const int num_tiles = num_mb * num_nb;
+  const int num_kt = args.K / Cfg::K_ELEMS;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, 2 * Cfg::EPI_THREADS);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSFA);
+    prefetch_tmap(&tmSFB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      const int64_t kc = (KIND == kMxf8) ? args.K / 128 : args.K / 64;  // 512-byte chunks per 128 rows
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+        int mb, nb;
+        tile_coords(tile, num_mb, num_nb, mb, nb);
+        const int a_row = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
+        const int b_row = nb * Cfg::BN + static_cast<int>(rank) * Cfg::ROWS;
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = map_to_rank(smem_u32(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+          tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmA, full_leader, kt * Cfg::KBYTES, a_row);
+          tma_load_2d_pair(sB + stage * Cfg::B_BYTES, &tmB, full_leader, kt * Cfg::KBYTES, b_row);
+          // 512-byte scale chunk (rb, c) starts at 128-byte row (rb * kc + c) * 4; a stage needs
+          // chunk c = kt (MX) or chunks 4kt .. 4kt+3 (NVFP4, contiguous; one 2 KB box)
+          const int64_t cfirst = (KIND == kMxf8) ? kt : 4ll * kt;
+          tma_load_2d_pair(sSFA + stage * Cfg::SFA_BYTES, &tmSFA, full_leader, 0,
+                           static_cast<int32_t>(((a_row / 128) * kc + cfirst) * 4));
+#pragma unroll
+          for (int rc = 0; rc < 2; ++rc)
+            tma_load_2d_pair(sSFB + stage * Cfg::SFB_BYTES + rc * Cfg::SF_CHUNK, &tmSFB, full_leader, 0,
+                             static_cast<int32_t>(((nb * 2 + rc) * kc + cfirst) * 4));
+          ++issued;
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: the leader's stage barriers count both CTAs' bytes, so the leader waits for every
+      // copy either CTA issued; the final cluster barrier keeps the peer alive until then
+      if (leader) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+          if (issued > s) {
+            const long last = s + ((issued - 1 - s) / Cfg::STAGES) * Cfg::STAGES;
+            mbar_wait(&full_bar[s], static_cast<uint32_t>((last / Cfg::STAGES) & 1), abort_flag, kSiteDrain);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      // The issue path of this single thread bounds the pair's throughput, so per k-step it does
+      // only: one barrier wait, the scale copies and MMAs with descriptor words advanced by
+      // constants, one commit.
+      constexpr uint32_t kOpHi = smem_desc_hi(1024, kSwizzle128B);
+      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
+      constexpr uint32_t kLbo = smem_desc_lo_lbo(16);
+      const uint32_t a_lo0 = (smem_u32(sA) >> 4) | kLbo, b_lo0 = (smem_u32(sB) >> 4) | kLbo;
+      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_it = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+        if (!mbar_wait(tempty_bar, (acc_it & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) break;
+        tc_fence_after();
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + stage * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + stage * (Cfg::B_BYTES >> 4);
+          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
+          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
+          const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
+          const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
+          if (KIND == kMxf8) {
+            tmem_cp_32x128b_warpx4_pair(sfa_t, desc_from_words(sfa_lo, kSfHi));
+            tmem_cp_32x128b_warpx4_pair(sfb_t, desc_from_words(sfb_lo, kSfHi));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, desc_from_words(sfb_lo + (512 >> 4), kSfHi));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
+              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j, desc_from_words(sfb_lo + j * (512 >> 4), kSfHi));
+              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4,
+                                          desc_from_words(sfb_lo + ((Cfg::SF_CHUNK + j * 512) >> 4), kSfHi));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < Cfg::NUM_MMA; ++j) {
+            const uint64_t adesc = desc_from_words(a_lo + j * 2, kOpHi);  // + 32 bytes of K per MMA
+            const uint64_t bdesc = desc_from_words(b_lo + j * 2, kOpHi);
+            const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
+            if (KIND == kMxf8)
+              umma_mxf8f6f4_pair(tmem_base, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), sfa_t, sfb_t, acc);
+            else
+              umma_mxf4nvf4_pair(tmem_base, adesc, bdesc, args.idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
+          }
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) {
+          umma_commit_pair(tfull_bar, 0x3);
+          ++acc_it;
+        }
+      }
+      umma_commit_pair(drain_bar, 0x1);
+      mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tempty_leader = map_to_rank(smem_u32(tempty_bar), 0);
+    constexpr int HALF = Cfg::BN / 2;
+    constexpr int NCH = HALF / 32;
+    float gscale = 1.0f;
+    if (KIND == kNvf4) gscale = __fmul_rn(*args.ga, *args.gb);
+    uint32_t acc_it = 0;
+    for (int tile = cluster; tile < num_tiles; tile += nclusters) {
+      int mb, nb;
+      tile_coords(tile, num_mb, num_nb, mb, nb);
+      bool ok = mbar_wait(tfull_bar, acc_it & 1, abort_flag, kSiteEpiTmemFull);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      uint32_t r[NCH][32];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tmem_ld_32x32b_x32(tmem_base + lane_addr + half * HALF + c * 32, r[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) tmem_regs_ready(r[c]);
+      tc_fence_before();
+      mbar_arrive_cluster(tempty_leader);
+      ++acc_it;
+      const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + rank * Cfg::ROWS + row_in_tile;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[c][i]), gscale) : __uint_as_float(r[c][i]);
+        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * Cfg::BN + half * HALF + c * 32, v);
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+}
+
+}  // namespace mxgb

@@ -67,11 +67,12 @@ def random_codes(rng, shape, fmt):
     return q
 
 
+@pytest.mark.parametrize("M", [128, 256])      # 128: single-CTA kernel; 256: CTA-pair kernel
 @pytest.mark.parametrize("K", [128, 256])
 @pytest.mark.parametrize("fa,fb", [(orc.E4M3, orc.E4M3), (orc.E5M2, orc.E4M3), (orc.E4M3, orc.E5M2), (orc.E5M2, orc.E5M2)])
-def test_mx_gemm_tiny_bruteforce(K, fa, fb):
-    rng = np.random.default_rng(K + 10 * fa + 100 * fb)
-    M, N = 128, 256
+def test_mx_gemm_tiny_bruteforce(M, K, fa, fb):
+    rng = np.random.default_rng(K + 10 * fa + 100 * fb + M)
+    N = 256
     qa, qb = random_codes(rng, (M, K), fa), random_codes(rng, (N, K), fb)
     sa = rng.integers(110, 145, (M, K // 32), dtype=np.uint8)
     sb = rng.integers(110, 145, (N, K // 32), dtype=np.uint8)
@@ -80,7 +81,7 @@ def test_mx_gemm_tiny_bruteforce(K, fa, fb):
     assert_close(y, ref, ab, what="tiny")
 
 
-@pytest.mark.parametrize("N", [128, 256])
+@pytest.mark.parametrize("N", [128, 256])       # 256 with M = 256: CTA-pair kernel
 def test_mx_gemm_one_hot_scale_probe(N):
     # all scales 2^0 except one (row r, k-block b) = 2^1: exactly the outputs of row r (or column
     # r for B) change, by that block's partial sum -- confirms the scale layout by behaviour
@@ -101,7 +102,7 @@ def test_mx_gemm_one_hot_scale_probe(N):
         ref, _ = orc.mx_gemm(qa, sa2, 0, qb, sb, 0, rows=[r])
         ref0, _ = orc.mx_gemm(qa, sa, 0, qb, sb, 0, rows=[r])
         assert np.allclose(d[r], (ref - ref0)[0], rtol=1e-6, atol=1e-6)
-    for (c, b) in [(0, 0), (77, 2), (N - 1, 7)]:
+    for (c, b) in [(0, 0), (77, 2), (N - 1, 7), (N // 2, 1), (N // 2 - 1, 6)]:
         sb2 = sb.copy()
         sb2[c, b] = 128
         y1 = run_mx(qa, sa, 0, qb, sb2, 0, M, N, K, mx.OUT_F32)
@@ -109,14 +110,16 @@ def test_mx_gemm_one_hot_scale_probe(N):
         assert changed.tolist() == [c], (c, b, changed[:10])
 
 
-def test_mx_gemm_one_hot_operand_probe():
+@pytest.mark.parametrize("M", [128, 256])
+def test_mx_gemm_one_hot_operand_probe(M):
     # a single nonzero code in A and B: the product lands in exactly one output
-    M, N, K = 128, 256, 256
+    N, K = 256, 256
     qa = np.zeros((M, K), np.uint8)
     qb = np.zeros((N, K), np.uint8)
     sa = np.full((M, K // 32), 127, np.uint8)
     sb = np.full((N, K // 32), 127, np.uint8)
-    for (m, n, k) in [(0, 0, 0), (5, 200, 77), (127, 255, 255), (64, 129, 130)]:
+    for (m, n, k) in [(0, 0, 0), (5, 200, 77), (M - 1, 255, 255), (64, 129, 130), (M // 2 + 3, 127, 31),
+                      (M - 40, 128, 128)]:
         qa[:] = 0
         qb[:] = 0
         qa[m, k] = 0x38   # 1.0
@@ -139,7 +142,8 @@ def test_mx_gemm_512_workload(out_dtype):
     assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="512^3")
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 640, 1024), (1152, 256, 2048)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 640, 1024), (1152, 256, 2048),
+                                   (256, 256, 128), (768, 1024, 640), (2560, 512, 384)])
 def test_mx_gemm_shapes(M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
     a = (torch.randn(M, K, generator=g) * 3).to(torch.bfloat16)
@@ -233,7 +237,8 @@ def test_nvfp4_scale_outside_sum_identity():
     assert y2[7, 9].item() == 7.875
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (512, 256, 2048)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (512, 256, 2048), (256, 256, 256),
+                                   (768, 512, 1024)])
 def test_nvfp4_gemm_random(M, N, K):
     a = synthetic.with_sparse_outliers(M, K, 4000 + M)
     b = synthetic.with_sparse_outliers(N, K, 4001 + N)
