@@ -67,7 +67,9 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = USED_COLS <= 32 ? 32 : USED_COLS <= 64 ? 64 : USED_COLS <= 128 ? 128
                                    : USED_COLS <= 256 ? 256 : 512;
   static constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of BN
-  static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+  static constexpr bool HAS_SF = (KIND != kDsF8);
+  static constexpr int SF_WARP = 2 + NUM_EPI_WARPS;  // issues the scale copies (block-scaled kinds)
+  static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS + (HAS_SF ? 32 : 0);
   static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
   static_assert(STAGES >= 2, "not enough shared memory for two stages");
   static_assert(USED_COLS <= 512, "TMEM overflow");
@@ -137,7 +139,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
   uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;       // [NBUF]
   uint64_t* tempty_bar = bars + 2 * Cfg::STAGES + 4;  // [NBUF]
   uint64_t* drain_bar = bars + 2 * Cfg::STAGES + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::STAGES + 9);
+  uint64_t* sfdrain_bar = bars + 2 * Cfg::STAGES + 9;
+  uint64_t* sfready_bar = bars + 2 * Cfg::STAGES + 10;  // [STAGES]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * Cfg::STAGES + 10);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -157,6 +161,8 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
       mbar_init(&tempty_bar[b], Cfg::EPI_THREADS);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(sfdrain_bar, 1);
+    for (int st = 0; st < Cfg::STAGES; ++st) mbar_init(&sfready_bar[st], 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -226,14 +232,13 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     // The issue path of this single thread bounds the CTA's throughput, so per k-step it does only:
-    // the barrier waits, the scale copies (into the stage's own TMEM columns) and MMAs with
-    // descriptor words advanced by constants, and the commits.
+    // the barrier waits, the MMAs with descriptor words advanced by constants, and the commits.
+    // The scale copies come from another warp: they overlap the MMAs only when a different thread
+    // issues them.
     if (lane == 0) {
       constexpr uint32_t kOpHi = smem_desc_hi(1024, kSwizzle128B);
-      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
       constexpr uint32_t kLbo = smem_desc_lo_lbo(16);
       const uint32_t a_lo0 = (smem_u32(sA) >> 4) | kLbo, b_lo0 = (smem_u32(sB) >> 4) | kLbo;
-      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_it = 0;  // accumulator hand-overs so far
@@ -254,32 +259,17 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
             tc_fence_after();
             d_tmem = tmem_base + b * BN;
           }
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+          // block-scaled kinds wait for the scale-copy warp's stage barrier (it follows the TMA
+          // barrier), the promotion kind for the TMA barrier itself
+          if (!mbar_wait(Cfg::HAS_SF ? &sfready_bar[stage] : &full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_lo = a_lo0 + stage * (Cfg::A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + stage * (Cfg::B_BYTES >> 4);
-          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
-          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
           const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
           const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
-          if (KIND == kMxf8) {
-            tmem_cp_32x128b_warpx4(sfa_t, desc_from_words(sfa_lo, kSfHi));
-#pragma unroll
-            for (int rc = 0; rc < Cfg::RC; ++rc)
-              tmem_cp_32x128b_warpx4(sfb_t + 4 * rc, desc_from_words(sfb_lo + rc * (512 >> 4), kSfHi));
-          } else if (KIND == kNvf4) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_warpx4(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
-#pragma unroll
-              for (int rc = 0; rc < Cfg::RC; ++rc)
-                tmem_cp_32x128b_warpx4(sfb_t + j * 4 * Cfg::RC + 4 * rc,
-                                       desc_from_words(sfb_lo + ((rc * 2048 + j * 512) >> 4), kSfHi));
-            }
-          }
 #pragma unroll
           for (int j = 0; j < Cfg::NUM_MMA; ++j) {
             const uint64_t adesc = desc_from_words(a_lo + j * 2, kOpHi);  // + 32 bytes of K per MMA
@@ -312,6 +302,51 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
       // drain: all MMAs issued by this thread complete before TMEM is released
       umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
+    }
+  } else if (Cfg::HAS_SF && warp == Cfg::SF_WARP) {
+    // ------------------------------------------------------------------ scale copies
+    if (lane == 0) {
+      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
+      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
+          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
+          const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
+          const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
+          if (KIND == kMxf8) {
+            tmem_cp_32x128b_warpx4(sfa_t, desc_from_words(sfa_lo, kSfHi));
+#pragma unroll
+            for (int rc = 0; rc < Cfg::RC; ++rc)
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * rc, desc_from_words(sfb_lo + rc * (512 >> 4), kSfHi));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
+#pragma unroll
+              for (int rc = 0; rc < Cfg::RC; ++rc)
+                tmem_cp_32x128b_warpx4(sfb_t + j * 4 * Cfg::RC + 4 * rc,
+                                       desc_from_words(sfb_lo + ((rc * 2048 + j * 512) >> 4), kSfHi));
+            }
+          }
+          umma_commit(&sfready_bar[stage]);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: every copy this thread issued completes before TMEM is released
+      umma_commit(sfdrain_bar);
+      mbar_wait(sfdrain_bar, 0, abort_flag, kSiteDrain);
     }
   } else {
     // ------------------------------------------------------------------ epilogue

@@ -48,7 +48,8 @@ struct Gemm2Cfg {
   static constexpr int SFB_COL = ACC_COLS + SFA_COLS;          // + stage * SF_STAGE_COLS
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_EPI_WARPS = 8;
-  static constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
+  static constexpr int SF_WARP = 2 + NUM_EPI_WARPS;  // issues the scale copies (leader CTA)
+  static constexpr int THREADS = 96 + 32 * NUM_EPI_WARPS;
   static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
   static_assert(STAGES >= 2, "not enough shared memory");
   static_assert(ACC_COLS + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM overflow");
@@ -74,7 +75,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
   uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;    // both CTAs
   uint64_t* tempty_bar = tfull_bar + 1;            // used in the leader
   uint64_t* drain_bar = tfull_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_bar + 3);
+  uint64_t* sfready_bar = tfull_bar + 3;           // [STAGES], used in the leader
+  uint64_t* sfdrain_bar = tfull_bar + 3 + Cfg::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_bar + 4 + Cfg::STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -96,6 +99,8 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 2 * Cfg::EPI_THREADS);
     mbar_init(drain_bar, 1);
+    for (int st = 0; st < Cfg::STAGES; ++st) mbar_init(&sfready_bar[st], 1);
+    mbar_init(sfdrain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -165,13 +170,12 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer (leader only)
     if (leader && lane == 0) {
       // The issue path of this single thread bounds the pair's throughput, so per k-step it does
-      // only: one barrier wait, the scale copies and MMAs with descriptor words advanced by
-      // constants, one commit.
+      // only: one barrier wait, the MMAs with descriptor words advanced by constants, one commit.
+      // The scale copies come from another warp (they overlap the MMAs only when a different
+      // thread issues them); its per-stage barrier also guarantees the stage's operands landed.
       constexpr uint32_t kOpHi = smem_desc_hi(1024, kSwizzle128B);
-      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
       constexpr uint32_t kLbo = smem_desc_lo_lbo(16);
       const uint32_t a_lo0 = (smem_u32(sA) >> 4) | kLbo, b_lo0 = (smem_u32(sB) >> 4) | kLbo;
-      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_it = 0;
@@ -180,30 +184,15 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
         if (!mbar_wait(tempty_bar, (acc_it & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         for (int kt = 0; kt < num_kt; ++kt) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+          if (!mbar_wait(&sfready_bar[stage], phase, abort_flag, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_lo = a_lo0 + stage * (Cfg::A_BYTES >> 4);
           const uint32_t b_lo = b_lo0 + stage * (Cfg::B_BYTES >> 4);
-          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
-          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
           const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
           const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
-          if (KIND == kMxf8) {
-            tmem_cp_32x128b_warpx4_pair(sfa_t, desc_from_words(sfa_lo, kSfHi));
-            tmem_cp_32x128b_warpx4_pair(sfb_t, desc_from_words(sfb_lo, kSfHi));
-            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, desc_from_words(sfb_lo + (512 >> 4), kSfHi));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
-              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j, desc_from_words(sfb_lo + j * (512 >> 4), kSfHi));
-              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4,
-                                          desc_from_words(sfb_lo + ((Cfg::SF_CHUNK + j * 512) >> 4), kSfHi));
-            }
-          }
 #pragma unroll
           for (int j = 0; j < Cfg::NUM_MMA; ++j) {
             const uint64_t adesc = desc_from_words(a_lo + j * 2, kOpHi);  // + 32 bytes of K per MMA
@@ -227,6 +216,49 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       }
       umma_commit_pair(drain_bar, 0x1);
       mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
+    }
+  } else if (warp == Cfg::SF_WARP) {
+    // ------------------------------------------------------------------ scale copies (leader only)
+    if (leader && lane == 0) {
+      constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
+      const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfa_lo = sfa_lo0 + stage * (Cfg::SFA_BYTES >> 4);
+          const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
+          const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
+          const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
+          if (KIND == kMxf8) {
+            tmem_cp_32x128b_warpx4_pair(sfa_t, desc_from_words(sfa_lo, kSfHi));
+            tmem_cp_32x128b_warpx4_pair(sfb_t, desc_from_words(sfb_lo, kSfHi));
+            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, desc_from_words(sfb_lo + (512 >> 4), kSfHi));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
+              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j, desc_from_words(sfb_lo + j * (512 >> 4), kSfHi));
+              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4,
+                                          desc_from_words(sfb_lo + ((Cfg::SF_CHUNK + j * 512) >> 4), kSfHi));
+            }
+          }
+          umma_commit_pair(&sfready_bar[stage], 0x1);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: every copy this thread issued completes before TMEM is released
+      umma_commit_pair(sfdrain_bar, 0x1);
+      mbar_wait(sfdrain_bar, 0, abort_flag, kSiteDrain);
     }
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
