@@ -139,10 +139,25 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
   if (!make_tmap(&tb, qb, args.N, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
   if (!make_tmap(&tsb, args.sfb, (args.N / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
+  // output tensor map: [M][ldc] elements, 32 x 32 boxes, swizzle matching the staging layout
+  CUtensorMap tout;
+  {
+    auto fn = get_encode_fn();
+    const size_t es = OUT_BF16 ? 2 : 4;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(args.N), static_cast<cuuint64_t>(args.M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(args.ldc * es)};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    if (!fn || fn(&tout, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, args.out,
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  OUT_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MX_ERR_CUDA;
+  }
   const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
   const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, args) != cudaSuccess) return MX_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, args) != cudaSuccess) return MX_ERR_CUDA;
   return launch_status();
 }
 

@@ -36,9 +36,12 @@ struct Gemm2Cfg {
   static constexpr int SFB_BYTES = 2 * SF_CHUNK;   // all 256 rows of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES) / STAGE_BYTES;
+  // output staging for the TMA stores: one 32 x 32 chunk (at most 4 KB) per epilogue warp, 1 KB
+  // aligned for the 128-byte swizzle
+  static constexpr int STAGING = 8 * 4096 + 1024;
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING + BAR_BYTES;
   static constexpr int NUM_MMA = KBYTES / 32;
   static constexpr int ACC_COLS = BN;
   static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : 16;
@@ -61,7 +64,7 @@ template <int KIND, bool OUT_BF16>
 __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                    const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
   using Cfg = Gemm2Cfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -69,7 +72,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
   uint8_t* sB = sA + Cfg::STAGES * Cfg::A_BYTES;
   uint8_t* sSFA = sB + Cfg::STAGES * Cfg::B_BYTES;
   uint8_t* sSFB = sSFA + Cfg::STAGES * Cfg::SFA_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES);
+  uint8_t* sOut = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sSFB + Cfg::STAGES * Cfg::SFB_BYTES + Cfg::STAGING);
   uint64_t* full_bar = bars;                       // [STAGES], used in the leader
   uint64_t* empty_bar = bars + Cfg::STAGES;        // [STAGES], both CTAs
   uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;    // both CTAs
@@ -107,6 +112,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmSFA);
     prefetch_tmap(&tmSFB);
+    prefetch_tmap(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -287,18 +293,49 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       tc_fence_before();
       mbar_arrive_cluster(tempty_leader);
       ++acc_it;
-      const int64_t row = static_cast<int64_t>(mb) * Cfg::BM + rank * Cfg::ROWS + row_in_tile;
+      // each 32 x 32 chunk goes through this warp's swizzled staging buffer and one TMA store
+      // (fewer, larger writes than per-thread vector stores, which slowed the MMA issue)
+      uint8_t* buf = sOut + (warp - 2) * 4096;
+      const int32_t y0 = static_cast<int32_t>(mb * Cfg::BM + rank * Cfg::ROWS + q * 32);
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[c][i]), gscale) : __uint_as_float(r[c][i]);
-        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * Cfg::BN + half * HALF + c * 32, v);
+        if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the buffer
+        __syncwarp();
+        if (OUT_BF16) {
+          // 32 rows x 64 B, 64-byte swizzle: 16-byte piece k of row r sits at piece k ^ ((r >> 1) & 3)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+              w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          // 32 rows x 128 B, 128-byte swizzle: piece k of row r sits at piece k ^ (r & 7)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmOut, buf, static_cast<int32_t>(nb * Cfg::BN + half * HALF + c * 32), y0);
+          bulk_commit_group();
+        }
       }
     }
   }
 
+  // the output stores complete before the CTA (and its staging buffers) goes away
+  if (warp >= 2 && warp < 2 + Cfg::NUM_EPI_WARPS && lane == 0) bulk_wait_all();
   tc_fence_before();
   cluster_sync_all();
   tc_fence_after();
