@@ -7,7 +7,7 @@ and every step of the computation runs in the library's CUDA kernels.  There
 is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
-  mx_quantize, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
+  mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
   mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
@@ -30,7 +30,7 @@ OUT_F32, OUT_BF16 = 0, 1
 EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
-    "nvfp4_quantize_noalloc",
+    "nvfp4_quantize_noalloc", "mx_quantize_dual",
 )
 
 
@@ -72,6 +72,7 @@ def load():
             "mx_check": (i32, [vp]),
             "mx_num_sms": (i32, []),
             "nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
+            "mx_quantize_dual": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -159,6 +160,28 @@ def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int
                             _ptr(q_col) if col else None, _ptr(s_col) if col else None, _stream(stream))
     _check(st, "mx_quantize")
     return (q_row if row else None, s_row if row else None, q_col if col else None, s_col if col else None)
+
+
+def mx_quantize_dual(x: torch.Tensor, layout: int = BOTH, e4m3=None, e5m2=None, stream=None):
+    """E4M3 and E5M2 MX quantization of bf16 x from one read (include/mx.h, mx_quantize_dual).
+    e4m3 / e5m2: optional (q_row, s_row, q_col, s_col) output tuples; returns both tuples."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    row, col = bool(layout & ROWWISE), bool(layout & COLWISE)
+
+    def alloc():
+        return (torch.empty(rows, cols, dtype=torch.uint8, device=dev) if row else None,
+                _u8(mx_scale_bytes(rows, cols), dev) if row else None,
+                torch.empty(cols, rows, dtype=torch.uint8, device=dev) if col else None,
+                _u8(mx_scale_bytes(cols, rows), dev) if col else None)
+    e4m3 = e4m3 if e4m3 is not None else alloc()
+    e5m2 = e5m2 if e5m2 is not None else alloc()
+    st = load().mx_quantize_dual(_ptr(x), rows, cols, layout, *[_ptr(t) for t in e4m3], *[_ptr(t) for t in e5m2],
+                                 _stream(stream))
+    _check(st, "mx_quantize_dual")
+    return e4m3, e5m2
 
 
 def nvfp4_quantize(x: torch.Tensor, q_packed=None, s_ue4m3=None, gscale=None, workspace=None, stream=None):

@@ -161,6 +161,30 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
   return launch_status();
 }
 
+// MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
+mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int f0, int nf, bool row, bool col,
+                             const MxOut& o, cudaStream_t st) {
+  const int64_t tiles = (rows / 128) * (cols / 128);
+  if (tiles > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(tiles));
+#define MXQ(F, N, R, C) mx_quantize_kernel<F, N, R, C><<<grid, 256, 0, st>>>(x, rows, cols, o)
+  if (nf == 2) {
+    if (row && col) MXQ(0, 2, true, true);
+    else if (row) MXQ(0, 2, true, false);
+    else MXQ(0, 2, false, true);
+  } else if (f0 == 0) {
+    if (row && col) MXQ(0, 1, true, true);
+    else if (row) MXQ(0, 1, true, false);
+    else MXQ(0, 1, false, true);
+  } else {
+    if (row && col) MXQ(1, 1, true, true);
+    else if (row) MXQ(1, 1, true, false);
+    else MXQ(1, 1, false, true);
+  }
+#undef MXQ
+  return launch_status();
+}
+
 bool gemm_shape_ok(int64_t M, int64_t N, int64_t K, int64_t kmult, int64_t ldc, mx_out od) {
   if (M <= 0 || N <= 0 || K <= 0) return false;
   if (M % 128 || N % 128 || K % kmult) return false;
@@ -216,24 +240,12 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     if (col && (!q_col || !s_col || !aligned(q_col, 16) || !aligned(s_col, 16))) return MX_ERR_INVALID_ARG;
     const int64_t tiles = (rows / 128) * (cols / 128);
     if (tiles > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-    const uint16_t* xb = static_cast<const uint16_t*>(x);
-    auto* qr = static_cast<uint8_t*>(q_row);
-    auto* sr = static_cast<uint8_t*>(s_row);
-    auto* qc = static_cast<uint8_t*>(q_col);
-    auto* sc = static_cast<uint8_t*>(s_col);
-    const dim3 grid(static_cast<unsigned>(tiles));
-#define MXQ(E, R, C) mx_quantize_kernel<E, R, C><<<grid, 256, 0, st>>>(xb, rows, cols, qr, sr, qc, sc)
-    if (elem == MX_E4M3) {
-      if (row && col) MXQ(0, true, true);
-      else if (row) MXQ(0, true, false);
-      else MXQ(0, false, true);
-    } else {
-      if (row && col) MXQ(1, true, true);
-      else if (row) MXQ(1, true, false);
-      else MXQ(1, false, true);
-    }
-#undef MXQ
-    return launch_status();
+    MxOut o{};
+    o.q_row[0] = static_cast<uint8_t*>(q_row);
+    o.s_row[0] = static_cast<uint8_t*>(s_row);
+    o.q_col[0] = static_cast<uint8_t*>(q_col);
+    o.s_col[0] = static_cast<uint8_t*>(s_col);
+    return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, elem == MX_E4M3 ? 0 : 1, 1, row, col, o, st);
   }
   if (block == 128 && sfmt == MX_SCALE_FP32 && elem == MX_E4M3 && layout == MX_ROWWISE &&
       (block_rows == 1 || block_rows == 128)) {
@@ -255,6 +267,32 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     return launch_status();
   }
   return MX_ERR_UNSUPPORTED;
+}
+
+mx_status mx_quantize_dual(const void* x, int64_t rows, int64_t cols, mx_layout layout, void* q_row_e4m3,
+                           void* s_row_e4m3, void* q_col_e4m3, void* s_col_e4m3, void* q_row_e5m2, void* s_row_e5m2,
+                           void* q_col_e5m2, void* s_col_e5m2, void* stream) {
+  if (!x || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MX_ERR_INVALID_ARG;
+  if (rows > (1ll << 31) || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
+  if (layout != MX_ROWWISE && layout != MX_COLWISE && layout != MX_BOTH) return MX_ERR_INVALID_ARG;
+  if (!aligned(x, 16)) return MX_ERR_INVALID_ARG;
+  const bool row = (layout & MX_ROWWISE) != 0, col = (layout & MX_COLWISE) != 0;
+  void* rp[4] = {q_row_e4m3, s_row_e4m3, q_row_e5m2, s_row_e5m2};
+  void* cp[4] = {q_col_e4m3, s_col_e4m3, q_col_e5m2, s_col_e5m2};
+  for (int i = 0; i < 4; ++i) {
+    if (row && (!rp[i] || !aligned(rp[i], 16))) return MX_ERR_INVALID_ARG;
+    if (col && (!cp[i] || !aligned(cp[i], 16))) return MX_ERR_INVALID_ARG;
+  }
+  MxOut o{};
+  o.q_row[0] = static_cast<uint8_t*>(q_row_e4m3);
+  o.s_row[0] = static_cast<uint8_t*>(s_row_e4m3);
+  o.q_col[0] = static_cast<uint8_t*>(q_col_e4m3);
+  o.s_col[0] = static_cast<uint8_t*>(s_col_e4m3);
+  o.q_row[1] = static_cast<uint8_t*>(q_row_e5m2);
+  o.s_row[1] = static_cast<uint8_t*>(s_row_e5m2);
+  o.q_col[1] = static_cast<uint8_t*>(q_col_e5m2);
+  o.s_col[1] = static_cast<uint8_t*>(s_col_e5m2);
+  return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, 0, 2, row, col, o, as_stream(stream));
 }
 
 mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb, int64_t M,

@@ -122,14 +122,26 @@ __device__ __forceinline__ uint32_t e2m1x2_quotient(float a, float b, const Quot
   return cvt_e2m1x2(__fdiv_rn(a, q.d), __fdiv_rn(b, q.d));
 }
 
-template <int ELEM, bool ROW, bool COL>
+// Output pointers of one MX quantize launch: up to two element formats (F0, then F0 + 1).
+struct MxOut {
+  uint8_t* q_row[2];
+  uint8_t* s_row[2];
+  uint8_t* q_col[2];
+  uint8_t* s_col[2];
+};
+
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_cvt2(float lo, float hi) {
+  return MxElem<FMT>::cvt2(lo, hi);
+}
+
+// NF = 1: format F0 only; NF = 2: E4M3 and E5M2 from the same read of x (F0 = 0).
+template <int F0, int NF, bool ROW, bool COL>
 __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                          int64_t cols, uint8_t* __restrict__ q_row,
-                                                          uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
-                                                          uint8_t* __restrict__ s_col) {
+                                                          int64_t cols, const MxOut o) {
   __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 1];  // 128 rows x 128 bf16 (as bf16x2 words)
-  __shared__ __align__(16) uint8_t srow[512];
-  __shared__ __align__(16) uint8_t scol[512];
+  __shared__ __align__(16) uint8_t srow[NF][512];
+  __shared__ __align__(16) uint8_t scol[NF][512];
 
   const int64_t tiles_c = cols >> 7;
   const int64_t tr = blockIdx.x / tiles_c;
@@ -156,17 +168,23 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
       uint32_t m = absmax_bits8(v[i]);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-      uint2 codes;
-      uint32_t sbyte;
-      if (m >= 0x7F80u) {  // NaN or Inf in the block
-        sbyte = 0xFF;
-        codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-      } else {
-        sbyte = mx_scale_byte<ELEM>(m);
-        codes = mx_codes8<ELEM>(v[i], mx_inv_scale(sbyte));
+#pragma unroll
+      for (int f = 0; f < NF; ++f) {
+        uint2 codes;
+        uint32_t sbyte;
+        if (m >= 0x7F80u) {  // NaN or Inf in the block
+          sbyte = 0xFF;
+          codes = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else if (F0 + f == 0) {
+          sbyte = mx_scale_byte<0>(m);
+          codes = mx_codes8<0>(v[i], mx_inv_scale(sbyte));
+        } else {
+          sbyte = mx_scale_byte<1>(m);
+          codes = mx_codes8<1>(v[i], mx_inv_scale(sbyte));
+        }
+        *reinterpret_cast<uint2*>(o.q_row[f] + (tr * 128 + r) * cols + tc * 128 + lc * 8) = codes;
+        if ((lc & 3) == 0) srow[f][chunk_offset(r, lc >> 2)] = static_cast<uint8_t>(sbyte);
       }
-      *reinterpret_cast<uint2*>(q_row + (tr * 128 + r) * cols + tc * 128 + lc * 8) = codes;
-      if ((lc & 3) == 0) srow[chunk_offset(r, lc >> 2)] = static_cast<uint8_t>(sbyte);
     }
   }
 
@@ -184,46 +202,51 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
       m1 = max(m1, (w[r] >> 16) & 0x7FFFu);
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t m = h ? m1 : m0;
-      const int c = 2 * p + h;  // column inside the tile = row of the transposed tile
-      uint32_t packed[8];
-      uint32_t sbyte;
-      if (m >= 0x7F80u) {
-        sbyte = 0xFF;
+    for (int f = 0; f < NF; ++f) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) packed[j] = 0x7F7F7F7Fu;
-      } else {
-        sbyte = mx_scale_byte<ELEM>(m);
-        const float inv = mx_inv_scale(sbyte);
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t m = h ? m1 : m0;
+        const int c = 2 * p + h;  // column inside the tile = row of the transposed tile
+        uint32_t packed[8];
+        uint32_t sbyte;
+        if (m >= 0x7F80u) {
+          sbyte = 0xFF;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int sh = h ? 16 : 0;
-          const float f0 = __fmul_rn(bf16_bits_to_float((w[4 * j + 0] >> sh) & 0xFFFFu), inv);
-          const float f1 = __fmul_rn(bf16_bits_to_float((w[4 * j + 1] >> sh) & 0xFFFFu), inv);
-          const float f2 = __fmul_rn(bf16_bits_to_float((w[4 * j + 2] >> sh) & 0xFFFFu), inv);
-          const float f3 = __fmul_rn(bf16_bits_to_float((w[4 * j + 3] >> sh) & 0xFFFFu), inv);
-          packed[j] = MxElem<ELEM>::cvt2(f0, f1) | (MxElem<ELEM>::cvt2(f2, f3) << 16);
+          for (int j = 0; j < 8; ++j) packed[j] = 0x7F7F7F7Fu;
+        } else {
+          sbyte = (F0 + f == 0) ? mx_scale_byte<0>(m) : mx_scale_byte<1>(m);
+          const float inv = mx_inv_scale(sbyte);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int sh = h ? 16 : 0;
+            const float f0 = __fmul_rn(bf16_bits_to_float((w[4 * j + 0] >> sh) & 0xFFFFu), inv);
+            const float f1 = __fmul_rn(bf16_bits_to_float((w[4 * j + 1] >> sh) & 0xFFFFu), inv);
+            const float f2 = __fmul_rn(bf16_bits_to_float((w[4 * j + 2] >> sh) & 0xFFFFu), inv);
+            const float f3 = __fmul_rn(bf16_bits_to_float((w[4 * j + 3] >> sh) & 0xFFFFu), inv);
+            packed[j] = (F0 + f == 0) ? (mx_cvt2<0>(f0, f1) | (mx_cvt2<0>(f2, f3) << 16))
+                                      : (mx_cvt2<1>(f0, f1) | (mx_cvt2<1>(f2, f3) << 16));
+          }
         }
+        uint8_t* dst = o.q_col[f] + (tc * 128 + c) * rows + tr * 128 + rb * 32;
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        scol[f][chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
       }
-      uint8_t* dst = q_col + (tc * 128 + c) * rows + tr * 128 + rb * 32;
-      reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-      scol[chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
     }
   }
 
   __syncthreads();
-  if (t < 32) {
-    if (ROW) {
-      uint8_t* dst = s_row + (tr * tiles_c + tc) * 512;
-      reinterpret_cast<uint4*>(dst)[t] = reinterpret_cast<const uint4*>(srow)[t];
-    }
-  } else if (t < 64) {
-    if (COL) {
+  // scale chunks: 32 threads per (format, copy), one 16-byte piece each
+  const int f = t >> 6;
+  const int u = t & 63;
+  if (f < NF) {
+    if (u < 32) {
+      uint8_t* srp = (NF == 1 || f == 0) ? o.s_row[0] : o.s_row[1];
+      if (ROW) reinterpret_cast<uint4*>(srp + (tr * tiles_c + tc) * 512)[u] = reinterpret_cast<const uint4*>(srow[f])[u];
+    } else if (COL) {
       const int64_t tiles_r = rows >> 7;
-      uint8_t* dst = s_col + (tc * tiles_r + tr) * 512;
-      reinterpret_cast<uint4*>(dst)[t - 32] = reinterpret_cast<const uint4*>(scol)[t - 32];
+      uint8_t* scp = (NF == 1 || f == 0) ? o.s_col[0] : o.s_col[1];
+      reinterpret_cast<uint4*>(scp + (tc * tiles_r + tr) * 512)[u - 32] = reinterpret_cast<const uint4*>(scol[f])[u - 32];
     }
   }
 }

@@ -102,6 +102,19 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
                       void* q_row, void* s_row, void* q_col, void* s_col, void* stream);
 
 /*
+ * mx_quantize_dual -- MX quantization of one bf16 matrix into both element formats at once:
+ * E4M3 and E5M2 codes with their E8M0 scales, row-wise and/or column-wise, from a single read of
+ * x.  Each output is exactly what mx_quantize (block = 32, MX_SCALE_E8M0) writes for that format.
+ * [MX] sec 0.1 (block format; E4M3 and E5M2 are both MXFP8 element encodings) and sec 1.2
+ * (row-wise and column-wise copies).  Shapes, alignment and layouts as in mx_quantize; the eight
+ * output pointers of the requested copies must be non-NULL.
+ */
+mx_status mx_quantize_dual(const void* x, int64_t rows, int64_t cols, mx_layout layout,
+                           void* q_row_e4m3, void* s_row_e4m3, void* q_col_e4m3, void* s_col_e4m3,
+                           void* q_row_e5m2, void* s_row_e5m2, void* q_col_e5m2, void* s_col_e5m2,
+                           void* stream);
+
+/*
  * mx_gemm -- MXFP8 block-scaled GEMM.  [MX] sec 0.3:
  *   C[m][n] = sum_b sA[m][b] sB[n][b] sum_{i<32} qA[m][32b+i] qB[n][32b+i], FP32 accumulate.
  *

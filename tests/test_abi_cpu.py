@@ -77,6 +77,21 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(elem=2) == mx.MX_ERR_UNSUPPORTED            # E2M1 with E8M0 (MXFP4) not built
 
 
+def test_dual_quantize_rejects_bad_arguments(lib):
+    d = lib.mx_quantize_dual
+    ptrs = [FAKE] * 8
+    # only argument combinations the host rejects: valid ones would launch on fake pointers
+    assert d(None, 256, 256, 3, *ptrs, None) == mx.MX_ERR_INVALID_ARG
+    assert d(FAKE, 200, 256, 3, *ptrs, None) == mx.MX_ERR_INVALID_ARG
+    assert d(FAKE, 256, 256, 0, *ptrs, None) == mx.MX_ERR_INVALID_ARG
+    bad = list(ptrs)
+    bad[6] = None                            # column-wise E5M2 codes missing
+    assert d(FAKE, 256, 256, 3, *bad, None) == mx.MX_ERR_INVALID_ARG
+    assert d(FAKE, 256, 256, 2, *bad, None) == mx.MX_ERR_INVALID_ARG
+    bad[1] = FAKE + 4                        # misaligned row-wise E4M3 scales
+    assert d(FAKE, 256, 256, 1, *bad, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_gemms_reject_bad_arguments(lib):
     g = lib.mx_gemm
     assert g(None, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG

@@ -96,6 +96,26 @@ def test_mx_outlier_workload_full_size(fmt):
     check_mx(x, fmt, layouts=(mx.BOTH,))
 
 
+@pytest.mark.parametrize("layout", [mx.BOTH, mx.ROWWISE, mx.COLWISE])
+def test_mx_dual_format_one_read_full_size(layout):
+    # both element formats from one read: every output equals the single-format oracle result
+    x = synthetic.mxfp8_quantize()          # 16384 x 4096
+    x[7, 9] = float("nan")
+    x[300, :32] = 0.0
+    rows, cols = x.shape
+    e4, e5 = mx.mx_quantize_dual(x.cuda(), layout=layout)
+    assert mx.mx_check() == mx.MX_OK
+    for fmt, out in ((orc.E4M3, e4), (orc.E5M2, e5)):
+        if layout & mx.ROWWISE:
+            oq, osc = orc.mx_quantize_rowwise(x, fmt)
+            assert np.array_equal(out[0].cpu().numpy(), oq)
+            assert np.array_equal(chunked_to_plain(out[1].cpu().numpy(), rows, cols // 32), osc)
+        if layout & mx.COLWISE:
+            oqT, osT = orc.mx_quantize_colwise(x, fmt)
+            assert np.array_equal(out[2].cpu().numpy(), oqT)
+            assert np.array_equal(chunked_to_plain(out[3].cpu().numpy(), cols, rows // 32), osT)
+
+
 @pytest.mark.parametrize("shape", [(128, 128), (256, 384), (384, 256), (1152, 640)])
 def test_mx_small_and_ragged_tile_counts(shape):
     g = torch.Generator().manual_seed(shape[0] * 7 + shape[1])
