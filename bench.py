@@ -323,6 +323,63 @@ def job_throughput(units_per_rank, world, ms_max):
     return world * units_per_rank / (ms_max / 1e3)
 
 
+def run_library_reference(args):
+    """Context only: cuBLASLt through torch._scaled_mm (and bf16 matmul) on the bench's GEMM
+    shapes, with random operands of the same types.  Prints one JSON line; never part of the
+    bench value and never on the product path."""
+    import torch
+    dev = torch.device("cuda")
+
+    def timeit(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    out = {"kind": "library_reference", "library": f"cuBLASLt via torch {torch.__version__}",
+           "device": torch.cuda.get_device_name(), "TFLOP/s": {}}
+    for (M, N, K) in [(8192, 14336, 4096), (8192, 4096, 14336), (14336, 4096, 8192), (8192, 8192, 8192),
+                      (4096, 2048, 7168)]:
+        fl = 2 * M * N * K
+        key = f"{M}x{N}x{K}"
+        res = {}
+        a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+        b = torch.randn(N, K, device=dev, dtype=torch.bfloat16)
+        res["bf16"] = round(fl / timeit(lambda: a @ b.t()) / 1e9, 1)
+        a8, b8 = a.to(torch.float8_e4m3fn), b.to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        try:
+            res["fp8_per_tensor"] = round(fl / timeit(lambda: torch._scaled_mm(
+                a8, b8.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)) / 1e9, 1)
+        except Exception as e:  # noqa: BLE001 -- report, do not fail
+            res["fp8_per_tensor"] = f"unavailable: {str(e)[:80]}"
+        try:
+            sa = torch.full((M * K // 32,), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+            sb = torch.full((N * K // 32,), 127, dtype=torch.uint8, device=dev).view(torch.float8_e8m0fnu)
+            res["mxfp8"] = round(fl / timeit(lambda: torch._scaled_mm(
+                a8, b8.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)) / 1e9, 1)
+        except Exception as e:  # noqa: BLE001
+            res["mxfp8"] = f"unavailable: {str(e)[:80]}"
+        try:
+            a4 = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+            b4 = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+            sa4 = torch.full((M * K // 16,), 0x38, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+            sb4 = torch.full((N * K // 16,), 0x38, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+            res["nvfp4"] = round(fl / timeit(lambda: torch._scaled_mm(
+                a4, b4.t(), scale_a=sa4, scale_b=sb4, out_dtype=torch.bfloat16)) / 1e9, 1)
+        except Exception as e:  # noqa: BLE001
+            res["nvfp4"] = f"unavailable: {str(e)[:80]}"
+        out["TFLOP/s"][key] = res
+    print(json.dumps(out))
+    return 0
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -360,12 +417,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--library-reference", action="store_true",
+                    help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
                     help="comma-separated subset of row groups (q2, lin, nv, ds) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.library_reference:
+        return run_library_reference(args)
     args.warmup = max(args.warmup, 3)
 
     rank, world, local = dist_env()

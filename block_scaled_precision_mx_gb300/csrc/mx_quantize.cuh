@@ -73,35 +73,40 @@ __device__ __forceinline__ uint2 mx_codes8(uint4 v, float inv) {
   return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
 }
 
+// largest |x| bit pattern (bf16 bits with the sign cleared) of 8 bf16 values; the two halves of
+// each word are compared as packed 16-bit unsigned integers
 __device__ __forceinline__ uint32_t absmax_bits8(uint4 v) {
-  uint32_t m = 0;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = max(m, w[i] & 0x7FFFu);
-    m = max(m, (w[i] >> 16) & 0x7FFFu);
-  }
-  return m;
+  uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
 }
 
 // ---------------------------------------------------------------------------------------------
 // Codes of fl32(x / d) without a per-element IEEE division.
 //
 // The recipes define the code as the rounding of the FP32 quotient fl32(x / d).  With
-// r = fl32(1 / d), the product x * r is within 1.5 FP32 ulp of fl32(x / d).  Converting
-// x * r * (1 - 2^-20) and x * r * (1 + 2^-20) brackets fl32(x / d); the conversions are monotonic,
+// r = rcp.approx(d) (relative error at most 1 ulp = 2^-23), x * r * (1 - 2^-19) and
+// x * r * (1 + 2^-19) bracket fl32(x / d) with room to spare; the conversions are monotonic,
 // so when both ends give the same code no rounding boundary of the format lies in between and
-// that code is the code of fl32(x / d).  When they differ (a boundary within ~2^-20 of the
+// that code is the code of fl32(x / d).  When they differ (a boundary within ~2^-19 of the
 // quotient, rare) the IEEE quotient decides.  The result is therefore identical to converting
 // __fdiv_rn(x, d).  `d` must be a normal float no larger than 2^125 (callers check).
 // ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+constexpr float kBracketDown = 1.0f - 1.9073486328125e-06f;  // 1 - 2^-19
+constexpr float kBracketUp = 1.0f + 1.9073486328125e-06f;    // 1 + 2^-19
+
 struct QuotientBracket {
-  float lo, hi;  // fl32(1/d) scaled by (1 - 2^-20) and (1 + 2^-20)
+  float lo, hi;  // rcp(d) scaled by (1 - 2^-19) and (1 + 2^-19)
   float d;
   __device__ __forceinline__ explicit QuotientBracket(float div) : d(div) {
-    const float r = __frcp_rn(div);
-    lo = __fmul_rn(r, 1.0f - 9.5367431640625e-07f);
-    hi = __fmul_rn(r, 1.0f + 9.5367431640625e-07f);
+    const float r = rcp_approx(div);
+    lo = __fmul_rn(r, kBracketDown);
+    hi = __fmul_rn(r, kBracketUp);
   }
   __device__ __forceinline__ static bool usable(float div) { return div >= 1.17549435e-38f && div <= 4.2535296e37f; }
 };
@@ -386,8 +391,17 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
   const uint4 v1 = ld_stream_v4(x + r * cols + c + 8);
   const uint32_t bm = max(absmax_bits8(v0), absmax_bits8(v1));
   const float bamax = bf16_bits_to_float(bm);
-  const float tq = __fdiv_rn(__fdiv_rn(bamax, 6.0f), sg);
-  const uint32_t scode = cvt_e4m3x2(tq, 0.0f) & 0xFFu;
+  // E4M3 code of t = fl32(fl32(bamax / 6) / s_g): bamax * fl32(1/6) * rcp(s_g) is within 2^-21 of
+  // t, so a +-2^-19 bracket that converts to one code decides it; otherwise the two IEEE quotients
+  uint32_t scode;
+  if (QuotientBracket::usable(sg)) {
+    const float y = __fmul_rn(__fmul_rn(bamax, 0.16666667163372040f), rcp_approx(sg));
+    const uint32_t c0 = cvt_e4m3x2(__fmul_rn(y, kBracketDown), 0.0f) & 0xFFu;
+    const uint32_t c1 = cvt_e4m3x2(__fmul_rn(y, kBracketUp), 0.0f) & 0xFFu;
+    scode = (c0 == c1) ? c0 : (cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu);
+  } else {
+    scode = cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu;
+  }
   const float s_hat = __fmul_rn(e4m3_to_float(scode), sg);
   const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   uint32_t lo = 0, hi = 0;
