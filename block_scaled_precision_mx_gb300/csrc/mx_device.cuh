@@ -391,3 +391,23 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA)
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 }  // namespace mxgb
+
+namespace mxgb {
+// Paired FP32 multiply-add on sm_100+: acc.{x,y} = s * p.{x,y} + acc.{x,y}, each element rounded
+// exactly as fmaf.  acc holds two floats as one 64-bit register pair.
+__device__ __forceinline__ void fma2_scalar(uint64_t& acc, uint64_t s2, uint32_t p_lo, uint32_t p_hi) {
+  asm("{\n\t.reg .b64 p;\n\t"
+      "mov.b64 p, {%1, %2};\n\t"
+      "fma.rn.f32x2 %0, %3, p, %0;\n\t}"
+      : "+l"(acc)
+      : "r"(p_lo), "r"(p_hi), "l"(s2));
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+}  // namespace mxgb

@@ -406,9 +406,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
           nsa1 = __ldg(sa_row + args.M);
           nsb1 = __ldg(sb_blk + 1);
         }
-        float acc[64];
+        uint64_t acc[32];  // 64 FP32 accumulators as pairs, updated with paired FMAs
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) acc[i] = 0ull;
         for (int kt = 0; kt < num_kt; kt += 2) {
           const bool two = kt + 1 < num_kt;
           const float s0 = __fmul_rn(nsa0, nsb0), s1 = __fmul_rn(nsa1, nsb1);
@@ -439,11 +439,12 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
           tc_fence_before();
           mbar_arrive(&tempty_bar[b0]);
           // the second k-block's TMEM loads overlap the first one's FMAs
+          const uint64_t s0x2 = pack_f32x2(s0, s0), s1x2 = pack_f32x2(s1, s1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[i] = fmaf(s0, __uint_as_float(r0[i]), acc[i]);
+          for (int i = 0; i < 16; ++i) fma2_scalar(acc[i], s0x2, r0[2 * i], r0[2 * i + 1]);
           if (two) tmem_ld_32x32b_x32(t1, r0);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s0, __uint_as_float(r1[i]), acc[32 + i]);
+          for (int i = 0; i < 16; ++i) fma2_scalar(acc[16 + i], s0x2, r1[2 * i], r1[2 * i + 1]);
           if (two) {
             tmem_ld_32x32b_x32(t1 + 32, r1);
             tmem_ld_wait();
@@ -452,15 +453,18 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
             tc_fence_before();
             mbar_arrive(&tempty_bar[b1]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = fmaf(s1, __uint_as_float(r0[i]), acc[i]);
+            for (int i = 0; i < 16; ++i) fma2_scalar(acc[i], s1x2, r0[2 * i], r0[2 * i + 1]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(s1, __uint_as_float(r1[i]), acc[32 + i]);
+            for (int i = 0; i < 16; ++i) fma2_scalar(acc[16 + i], s1x2, r1[2 * i], r1[2 * i + 1]);
           }
           acc_it += two ? 2 : 1;
         }
         if (!ok) break;
-        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64, acc);
-        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64 + 32, acc + 32);
+        float accf[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) unpack_f32x2(acc[i], accf[2 * i], accf[2 * i + 1]);
+        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64, accf);
+        store_row32<OUT_BF16>(args.out, args.ldc, row, static_cast<int64_t>(nb) * BN + half * 64 + 32, accf + 32);
       }
     }
   }

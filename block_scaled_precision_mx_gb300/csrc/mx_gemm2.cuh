@@ -51,8 +51,11 @@ struct Gemm2Cfg {
   static constexpr int SFB_COL = ACC_COLS + SFA_COLS;          // + stage * SF_STAGE_COLS
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_EPI_WARPS = 8;
-  static constexpr int SF_WARP = 2 + NUM_EPI_WARPS;  // issues the scale copies (leader CTA)
-  static constexpr int THREADS = 96 + 32 * NUM_EPI_WARPS;
+  // warps SF_WARP .. SF_WARP + SF_ISSUERS - 1 issue the scale copies (leader CTA): one thread
+  // cannot issue the twelve NVFP4 copies of a stage as fast as the MMAs consume them
+  static constexpr int SF_WARP = 2 + NUM_EPI_WARPS;
+  static constexpr int SF_ISSUERS = 2;
+  static constexpr int THREADS = 64 + 32 * SF_ISSUERS + 32 * NUM_EPI_WARPS;
   static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
   static_assert(STAGES >= 2, "not enough shared memory");
   static_assert(ACC_COLS + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM overflow");
@@ -104,8 +107,8 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     mbar_init(tfull_bar, 1);
     mbar_init(tempty_bar, 2 * Cfg::EPI_THREADS);
     mbar_init(drain_bar, 1);
-    for (int st = 0; st < Cfg::STAGES; ++st) mbar_init(&sfready_bar[st], 1);
-    mbar_init(sfdrain_bar, 1);
+    for (int st = 0; st < Cfg::STAGES; ++st) mbar_init(&sfready_bar[st], Cfg::SF_ISSUERS);
+    mbar_init(sfdrain_bar, Cfg::SF_ISSUERS);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -223,8 +226,11 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       umma_commit_pair(drain_bar, 0x1);
       mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
     }
-  } else if (warp == Cfg::SF_WARP) {
+  } else if (warp >= Cfg::SF_WARP) {
     // ------------------------------------------------------------------ scale copies (leader only)
+    // Per stage and MMA j there are three 512-byte chunk copies: A's scales, then B's scales for
+    // rows 0-127 and 128-255.  Copy c = 3j + w goes to issuer c % SF_ISSUERS.
+    const int part = warp - Cfg::SF_WARP;
     if (leader && lane == 0) {
       constexpr uint32_t kSfHi = smem_desc_hi(128, kSwizzleNone);
       const uint32_t sfa_lo0 = smem_u32(sSFA) >> 4, sfb_lo0 = smem_u32(sSFB) >> 4;
@@ -242,18 +248,16 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
           const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
           const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
           const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
-          if (KIND == kMxf8) {
-            tmem_cp_32x128b_warpx4_pair(sfa_t, desc_from_words(sfa_lo, kSfHi));
-            tmem_cp_32x128b_warpx4_pair(sfb_t, desc_from_words(sfb_lo, kSfHi));
-            tmem_cp_32x128b_warpx4_pair(sfb_t + 4, desc_from_words(sfb_lo + (512 >> 4), kSfHi));
-          } else {
+          // an MXFP8 stage's one MMA group reads one chunk of each scale tensor (its four MMAs
+          // pick bytes with the scale ids); an NVFP4 stage has a chunk per MMA
+          constexpr int NCOPY = (KIND == kMxf8) ? 3 : 3 * Cfg::NUM_MMA;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_warpx4_pair(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
-              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j, desc_from_words(sfb_lo + j * (512 >> 4), kSfHi));
-              tmem_cp_32x128b_warpx4_pair(sfb_t + 8 * j + 4,
-                                          desc_from_words(sfb_lo + ((Cfg::SF_CHUNK + j * 512) >> 4), kSfHi));
-            }
+          for (int c = 0; c < NCOPY; ++c) {
+            if (c % Cfg::SF_ISSUERS != part) continue;
+            const int j = c / 3, w = c % 3;
+            const uint32_t taddr = (w == 0) ? sfa_t + 4 * j : sfb_t + 8 * j + 4 * (w - 1);
+            const uint32_t lo = (w == 0) ? sfa_lo + j * (512 >> 4) : sfb_lo + (((w - 1) * Cfg::SF_CHUNK + j * 512) >> 4);
+            tmem_cp_32x128b_warpx4_pair(taddr, desc_from_words(lo, kSfHi));
           }
           umma_commit_pair(&sfready_bar[stage], 0x1);
           if (++stage == Cfg::STAGES) {
@@ -270,7 +274,6 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int row_in_tile = q * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tempty_leader = map_to_rank(smem_u32(tempty_bar), 0);
     constexpr int HALF = Cfg::BN / 2;
