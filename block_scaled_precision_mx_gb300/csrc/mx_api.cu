@@ -104,12 +104,27 @@ mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const Gemm
   return launch_status();
 }
 
-// CTA-pair kernel: clusters of two CTAs, each pair computing 256 x 256 output tiles.
-template <int KIND, bool OUT_BF16>
-mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
-  using Cfg = Gemm2Cfg<KIND>;
-  auto kern = bs_gemm2_kernel<KIND, OUT_BF16>;
-  static int max_clusters[64] = {};
+// Output tensor map: [M][ldc] elements, 32 x 32 boxes, swizzle matching the epilogues' staging
+// layout (64-byte rows for bf16, 128-byte rows for FP32).
+bool make_out_tmap(CUtensorMap* map, void* out, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const size_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * es)};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch a CTA-pair kernel: clusters of two CTAs, as many clusters as fit on the device at once
+// (each persistent over its share of `tiles`).  `max_clusters` caches the occupancy per device
+// for this kernel.
+template <typename... KArgs, typename... Args>
+mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int tiles, int (&max_clusters)[64],
+                       cudaStream_t st, Args... args) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -118,13 +133,13 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(Cfg::THREADS);
-  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_clusters[dev] == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
       return MX_ERR_CUDA;
     const int sms = device_sms();
     cfg.gridDim = dim3(static_cast<unsigned>(sms - (sms & 1)));
@@ -132,33 +147,28 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return MX_ERR_CUDA;
     max_clusters[dev] = n;
   }
+  const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return MX_ERR_CUDA;
+  return launch_status();
+}
+
+// Block-scaled CTA-pair kernel, 256 x 256 output tiles.
+template <int KIND, bool OUT_BF16>
+mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
+  using Cfg = Gemm2Cfg<KIND>;
+  static int max_clusters[64] = {};
   const int64_t kc = (KIND == kMxf8) ? args.K / 128 : args.K / 64;
   const int chunk_rows = Cfg::SF_CHUNK / 128;
-  CUtensorMap ta, tb, tsa, tsb;
+  CUtensorMap ta, tb, tsa, tsb, tout;
   if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tb, qb, args.N, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
   if (!make_tmap(&tsb, args.sfb, (args.N / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
-  // output tensor map: [M][ldc] elements, 32 x 32 boxes, swizzle matching the staging layout
-  CUtensorMap tout;
-  {
-    auto fn = get_encode_fn();
-    const size_t es = OUT_BF16 ? 2 : 4;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(args.N), static_cast<cuuint64_t>(args.M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(args.ldc * es)};
-    cuuint32_t box[2] = {32u, 32u};
-    cuuint32_t estr[2] = {1u, 1u};
-    if (!fn || fn(&tout, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, args.out,
-                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  OUT_BF16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MX_ERR_CUDA;
-  }
+  if (!make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)) return MX_ERR_CUDA;
   const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
-  const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, args) != cudaSuccess) return MX_ERR_CUDA;
-  return launch_status();
+  return launch_pairs(bs_gemm2_kernel<KIND, OUT_BF16>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters, st, ta,
+                      tb, tsa, tsb, tout, args);
 }
 
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
@@ -401,8 +411,8 @@ mx_status fp8_blockwise_gemm(const void* qa, const float* sa, const void* qb, co
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.idesc = make_idesc_f8f6f4(0u, 0u, 128, 128);
   cudaStream_t st = as_stream(stream);
+  a.idesc = make_idesc_f8f6f4(0u, 0u, 128, 128);
   if (out_dtype == MX_OUT_BF16) return launch_gemm<kDsF8, 128, true>(qa, qb, K, a, st);
   return launch_gemm<kDsF8, 128, false>(qa, qb, K, a, st);
 }

@@ -22,6 +22,42 @@
 
 namespace mxgb {
 
+// Write one warp's 32 x 32 output chunk (row = lane, 32 consecutive columns in v) through its
+// swizzled staging buffer and one TMA tensor store at (x, y) -- fewer, larger writes than
+// per-thread vector stores, which slowed the MMA issue.  The buffer is reused only after the
+// previous store has read it.
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_chunk_32x32(const CUtensorMap* tmOut, uint8_t* buf, const float (&v)[32],
+                                                  int lane, int32_t x, int32_t y) {
+  if (lane == 0) bulk_wait_read_all();
+  __syncwarp();
+  if (OUT_BF16) {
+    // 32 rows x 64 B, 64-byte swizzle: 16-byte piece k of row r sits at piece k ^ ((r >> 1) & 3)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    // 32 rows x 128 B, 128-byte swizzle: piece k of row r sits at piece k ^ (r & 7)
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<float4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmOut, buf, x, y);
+    bulk_commit_group();
+  }
+}
+
 template <int KIND>
 struct Gemm2Cfg {
   static constexpr int BM = 256;       // rows per pair tile (128 per CTA)
@@ -306,33 +342,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[c][i]), gscale) : __uint_as_float(r[c][i]);
-        if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the buffer
-        __syncwarp();
-        if (OUT_BF16) {
-          // 32 rows x 64 B, 64-byte swizzle: 16-byte piece k of row r sits at piece k ^ ((r >> 1) & 3)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
-              w[e] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
-          // 32 rows x 128 B, 128-byte swizzle: piece k of row r sits at piece k ^ (r & 7)
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4*>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmOut, buf, static_cast<int32_t>(nb * Cfg::BN + half * HALF + c * 32), y0);
-          bulk_commit_group();
-        }
+        store_chunk_32x32<OUT_BF16>(&tmOut, buf, v, lane, static_cast<int32_t>(nb * Cfg::BN + half * HALF + c * 32), y0);
       }
     }
   }

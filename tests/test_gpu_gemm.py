@@ -284,6 +284,45 @@ def test_deepseek_gemm_small(M, N, K):
     assert_close(y.cpu().numpy(), ref, ab, what="deepseek")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (512, 768, 1024), (768, 512, 256)])
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_deepseek_gemm_more_shapes(M, N, K, out_dtype):
+    # several tiles in both directions, a single k-block (K = 128) and an odd k-block count
+    a = synthetic.normal(M, K, 1.0, 5100 + K)
+    b = synthetic.normal(N, K, 0.02, 5101 + K)
+    y, qa, sa, qb, sb = ds_run(a, b, out_dtype=out_dtype)
+    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="deepseek shapes")
+
+
+def test_deepseek_gemm_scale_per_block():
+    # magnitudes that differ per row, per 128-column block of B and per k-block, so a scale taken
+    # from the wrong row, N-block or k-block (or applied to the wrong TMEM buffer) shows
+    M, N, K = 512, 512, 768
+    a = synthetic.normal(M, K, 1.0, 5200)
+    b = synthetic.normal(N, K, 1.0, 5201)
+    ra = 2.0 ** (torch.arange(M) % 9 - 4).float()
+    ka = 2.0 ** (torch.arange(K) // 128 * 3 - 6).float()
+    nb_ = 2.0 ** (torch.arange(N) // 128 * 2 - 3).float()
+    kb = 2.0 ** (5 - torch.arange(K) // 128 * 2).float()
+    a = (a.float() * ra[:, None] * ka[None, :]).to(torch.bfloat16)
+    b = (b.float() * nb_[:, None] * kb[None, :]).to(torch.bfloat16)
+    y, qa, sa, qb, sb = ds_run(a, b)
+    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    assert_close(y.cpu().numpy(), ref, ab, what="deepseek scales")
+
+
+def test_deepseek_gemm_more_tiles_than_sms():
+    # 1024 tiles of 128 x 128: every CTA runs several tiles, the buffers' phases wrap many times
+    M, N, K = 4096, 4096, 384
+    a = synthetic.normal(M, K, 1.0, 5300)
+    b = synthetic.normal(N, K, 0.05, 5301)
+    y, qa, sa, qb, sb = ds_run(a, b)
+    rows = np.array([0, 255, 256, 1031, 2048, 3333, 4095])
+    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy(), rows=rows)
+    assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="deepseek tiles")
+
+
 def test_deepseek_gemm_full_size():
     a, b = synthetic.deepseek_pair()
     M, K = a.shape
