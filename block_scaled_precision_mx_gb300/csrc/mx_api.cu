@@ -172,11 +172,18 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
 }
 
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
+// Quantizer grids are 2-D, x = row tiles (< 2^31), y = column tiles (at most 65535), so that no
+// thread divides 64-bit integers to find its tile.
+bool quant_grid(int64_t row_tiles, int64_t col_tiles, dim3* g) {
+  if (row_tiles <= 0 || col_tiles <= 0 || row_tiles > 0x7FFFFFFFll || col_tiles > 65535) return false;
+  *g = dim3(static_cast<unsigned>(row_tiles), static_cast<unsigned>(col_tiles));
+  return true;
+}
+
 mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int f0, int nf, bool row, bool col,
                              const MxOut& o, cudaStream_t st) {
-  const int64_t tiles = (rows / 128) * (cols / 128);
-  if (tiles > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-  const dim3 grid(static_cast<unsigned>(tiles));
+  dim3 grid;
+  if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
 #define MXQ(F, N, R, C) mx_quantize_kernel<F, N, R, C><<<grid, 256, 0, st>>>(x, rows, cols, o)
   if (nf == 2) {
     if (row && col) MXQ(0, 2, true, true);
@@ -262,15 +269,15 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     if (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 4)) return MX_ERR_INVALID_ARG;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     if (block_rows == 1) {
-      const int64_t ctas = (rows / 64) * (cols / 128);
-      if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-      ds_quantize_1x128_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(xb, rows, cols,
+      dim3 grid;
+      if (!quant_grid(rows / 64, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
+      ds_quantize_1x128_kernel<<<grid, 256, 0, st>>>(xb, rows, cols,
                                                                             static_cast<uint8_t*>(q_row),
                                                                             static_cast<float*>(s_row));
     } else {
-      const int64_t ctas = (rows / 128) * (cols / 128);
-      if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-      ds_quantize_128x128_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(xb, rows, cols,
+      dim3 grid;
+      if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
+      ds_quantize_128x128_kernel<<<grid, 256, 0, st>>>(xb, rows, cols,
                                                                               static_cast<uint8_t*>(q_row),
                                                                               static_cast<float*>(s_row));
     }
@@ -359,9 +366,9 @@ mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* q_pack
   if (grid1 > 8ll * sms) grid1 = 8ll * sms;
   nvfp4_amax_kernel<<<static_cast<unsigned>(grid1), 256, 0, st>>>(static_cast<const uint16_t*>(x), nvec, amax);
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
-  const int64_t ctas = (rows / 32) * ((cols + 127) / 128);
-  if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(static_cast<const uint16_t*>(x), rows, cols,
+  dim3 grid;
+  if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), rows, cols,
                                                                       static_cast<uint8_t*>(q_packed),
                                                                       static_cast<uint8_t*>(s_ue4m3), gscale, amax);
   return launch_status();
@@ -523,9 +530,9 @@ extern "C" mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
   nvfp4_amax_finalize_kernel<<<1, 1024, 0, st>>>(scratch, nbands, scratch + kNoAllocSlots);
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
-  const int64_t ctas = (rows / 32) * ((cols + 127) / 128);
-  if (ctas > 0x7FFFFFFFll) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_kernel<<<static_cast<unsigned>(ctas), 256, 0, st>>>(
+  dim3 grid;
+  if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_kernel<<<grid, 256, 0, st>>>(
       static_cast<const uint16_t*>(x), rows, cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3),
       gscale, scratch + kNoAllocSlots);
   return launch_status();

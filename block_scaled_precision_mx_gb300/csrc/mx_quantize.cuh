@@ -141,16 +141,18 @@ __device__ __forceinline__ uint32_t mx_cvt2(float lo, float hi) {
 }
 
 // NF = 1: format F0 only; NF = 2: E4M3 and E5M2 from the same read of x (F0 = 0).
+// Four resident CTAs per SM (64 registers a thread) keep enough loads in flight.
 template <int F0, int NF, bool ROW, bool COL>
-__global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, const MxOut o) {
   __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 1];  // 128 rows x 128 bf16 (as bf16x2 words)
   __shared__ __align__(16) uint8_t srow[NF][512];
   __shared__ __align__(16) uint8_t scol[NF][512];
 
+  // grid: x = row tile, y = column tile (no 64-bit division per thread)
   const int64_t tiles_c = cols >> 7;
-  const int64_t tr = blockIdx.x / tiles_c;
-  const int64_t tc = blockIdx.x % tiles_c;
+  const int64_t tr = blockIdx.x;
+  const int64_t tc = blockIdx.y;
   const int t = threadIdx.x;
   const int lc = t & 15;     // 16 threads per row, 8 bf16 (one uint4) each
   const int r0 = t >> 4;     // rows r0 + 16*i
@@ -195,47 +197,56 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
 
   if (COL) {
     __syncthreads();
-    // thread -> (column pair p, row block rb): reads one bf16x2 word per row of its block
-    const int p = t & 63;
+    // thread -> (column quad cq, row block rb, half hb): 16 rows x 4 columns, two bf16x2 words
+    // (one conflict-free 8-byte shared load) per row; the partner thread (lane ^ 1) holds the
+    // block's other 16 rows
+    const int lane = t & 31;
+    const int hb = lane & 1;
+    const int cq = (lane >> 1) + 16 * ((t >> 5) & 1);
     const int rb = t >> 6;
-    uint32_t w[32];
-    uint32_t m0 = 0, m1 = 0;
+    uint2 u[16];
+    uint32_t m[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      w[r] = tile[(rb * 32 + r) * 64 + p];
-      m0 = max(m0, w[r] & 0x7FFFu);
-      m1 = max(m1, (w[r] >> 16) & 0x7FFFu);
+    for (int r = 0; r < 16; ++r) {
+      u[r] = *reinterpret_cast<const uint2*>(&tile[(rb * 32 + hb * 16 + r) * 64 + 2 * cq]);
+      m[0] = max(m[0], u[r].x & 0x7FFFu);
+      m[1] = max(m[1], (u[r].x >> 16) & 0x7FFFu);
+      m[2] = max(m[2], u[r].y & 0x7FFFu);
+      m[3] = max(m[3], (u[r].y >> 16) & 0x7FFFu);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m[j] = max(m[j], __shfl_xor_sync(0xFFFFFFFFu, m[j], 1));
 #pragma unroll
     for (int f = 0; f < NF; ++f) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t m = h ? m1 : m0;
-        const int c = 2 * p + h;  // column inside the tile = row of the transposed tile
-        uint32_t packed[8];
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * cq + j;  // column inside the tile = row of the transposed tile
+        uint32_t packed[4];
         uint32_t sbyte;
-        if (m >= 0x7F80u) {
+        if (m[j] >= 0x7F80u) {  // NaN or Inf in the block
           sbyte = 0xFF;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) packed[j] = 0x7F7F7F7Fu;
+          for (int k = 0; k < 4; ++k) packed[k] = 0x7F7F7F7Fu;
         } else {
-          sbyte = (F0 + f == 0) ? mx_scale_byte<0>(m) : mx_scale_byte<1>(m);
+          sbyte = (F0 + f == 0) ? mx_scale_byte<0>(m[j]) : mx_scale_byte<1>(m[j]);
           const float inv = mx_inv_scale(sbyte);
+          const int sh = (j & 1) ? 16 : 0;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int sh = h ? 16 : 0;
-            const float f0 = __fmul_rn(bf16_bits_to_float((w[4 * j + 0] >> sh) & 0xFFFFu), inv);
-            const float f1 = __fmul_rn(bf16_bits_to_float((w[4 * j + 1] >> sh) & 0xFFFFu), inv);
-            const float f2 = __fmul_rn(bf16_bits_to_float((w[4 * j + 2] >> sh) & 0xFFFFu), inv);
-            const float f3 = __fmul_rn(bf16_bits_to_float((w[4 * j + 3] >> sh) & 0xFFFFu), inv);
-            packed[j] = (F0 + f == 0) ? (mx_cvt2<0>(f0, f1) | (mx_cvt2<0>(f2, f3) << 16))
+          for (int k = 0; k < 4; ++k) {
+            uint32_t e[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) e[i] = ((j < 2) ? u[4 * k + i].x : u[4 * k + i].y) >> sh;
+            const float f0 = __fmul_rn(bf16_bits_to_float(e[0] & 0xFFFFu), inv);
+            const float f1 = __fmul_rn(bf16_bits_to_float(e[1] & 0xFFFFu), inv);
+            const float f2 = __fmul_rn(bf16_bits_to_float(e[2] & 0xFFFFu), inv);
+            const float f3 = __fmul_rn(bf16_bits_to_float(e[3] & 0xFFFFu), inv);
+            packed[k] = (F0 + f == 0) ? (mx_cvt2<0>(f0, f1) | (mx_cvt2<0>(f2, f3) << 16))
                                       : (mx_cvt2<1>(f0, f1) | (mx_cvt2<1>(f2, f3) << 16));
           }
         }
-        uint8_t* dst = o.q_col[f] + (tc * 128 + c) * rows + tr * 128 + rb * 32;
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        scol[f][chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
+        uint8_t* dst = o.q_col[f] + (tc * 128 + c) * rows + tr * 128 + rb * 32 + hb * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if (hb == 0) scol[f][chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
       }
     }
   }
@@ -264,9 +275,8 @@ __global__ void __launch_bounds__(256) mx_quantize_kernel(const uint16_t* __rest
 __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ q,
                                                                 float* __restrict__ s) {
-  const int64_t kb_count = cols >> 7;
-  const int64_t kb = blockIdx.x % kb_count;
-  const int64_t rgrp = blockIdx.x / kb_count;
+  const int64_t kb = blockIdx.y;    // grid: x = group of 64 rows, y = k-block
+  const int64_t rgrp = blockIdx.x;
   const int t = threadIdx.x;
   const int lc = t & 15;
   uint4 v[4];
@@ -306,7 +316,7 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
                                                                   float* __restrict__ s) {
   __shared__ uint32_t wmax[8];
   const int64_t nbc = cols >> 7;
-  const int64_t br = blockIdx.x / nbc, bc = blockIdx.x % nbc;
+  const int64_t br = blockIdx.x, bc = blockIdx.y;  // grid: x = block row, y = block column
   const int t = threadIdx.x;
   const int lc = t & 15, r0 = t >> 4;
   const uint16_t* xb = x + (br * 128) * cols + bc * 128;
@@ -376,9 +386,9 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
                                                              int64_t cols, uint8_t* __restrict__ qp,
                                                              uint8_t* __restrict__ sf, float* __restrict__ gscale,
                                                              const unsigned int* __restrict__ amax_bits) {
-  // column tiles of 128; the last one may be half full (cols % 128 == 64)
-  const int64_t tiles_c = (cols + 127) >> 7;
-  const int64_t tr = blockIdx.x / tiles_c, tc = blockIdx.x % tiles_c;
+  // grid: x = 32-row tile, y = 128-column tile; the last column tile may be half full
+  // (cols % 128 == 64)
+  const int64_t tr = blockIdx.x, tc = blockIdx.y;
   const int t = threadIdx.x;
   const int64_t r = tr * 32 + (t >> 3);
   const int64_t c = tc * 128 + (t & 7) * 16;

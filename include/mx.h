@@ -15,7 +15,8 @@
  *  - Arguments are validated on the host before anything is launched.  A null pointer, a
  *    shape that is not a multiple of the tile, a misaligned pointer or a bad enum value
  *    returns MX_ERR_INVALID_ARG; a valid but unimplemented combination returns
- *    MX_ERR_UNSUPPORTED; a launch failure returns MX_ERR_CUDA.
+ *    MX_ERR_UNSUPPORTED; a launch failure returns MX_ERR_CUDA.  The quantizers take at most
+ *    65535 tiles of 128 columns (cols <= 8388480); wider inputs return MX_ERR_INVALID_ARG.
  *  - Device-side waits are bounded.  A wait that runs out sets a device error word instead of
  *    hanging; mx_check() reports it as MX_ERR_TIMEOUT.
  *

@@ -75,6 +75,7 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(block=64) == mx.MX_ERR_UNSUPPORTED
     assert call(block=128, sfmt=2, layout=2) == mx.MX_ERR_UNSUPPORTED   # DeepSeek column-wise
     assert call(elem=2) == mx.MX_ERR_UNSUPPORTED            # E2M1 with E8M0 (MXFP4) not built
+    assert call(rows=128, cols=65536 * 128) == mx.MX_ERR_INVALID_ARG   # more than 65535 column tiles
 
 
 def test_dual_quantize_rejects_bad_arguments(lib):
