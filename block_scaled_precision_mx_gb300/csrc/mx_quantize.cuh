@@ -269,45 +269,40 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
 
 // ---------------------------------------------------------------------------------------------
 // DeepSeek 1x128: s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored
-// [K/128][rows].  CTA = 64 rows x one 128-column k-block; 16 lanes per row, 8 bf16 per lane
-// (one 128-bit load), the row maximum reduced over the 16 lanes of a half warp.
+// [K/128][rows].  CTA = 64 rows x one 128-column k-block; 4 lanes per row, 32 bf16 per lane (four
+// 128-bit loads, the row's 4 lanes covering 64 contiguous bytes per load), so the per-row scale
+// and reciprocal are computed by 4 lanes, not 16.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ q,
                                                                 float* __restrict__ s) {
-  const int64_t kb = blockIdx.y;    // grid: x = group of 64 rows, y = k-block
-  const int64_t rgrp = blockIdx.x;
+  const int64_t kb = blockIdx.y;  // grid: x = group of 64 rows, y = k-block
   const int t = threadIdx.x;
-  const int lc = t & 15;
+  const int l4 = t & 3;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 64 + (t >> 2);
+  const uint16_t* xr = x + r * cols + kb * 128;
   uint4 v[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t r = rgrp * 64 + (t >> 4) + 16 * i;
-    v[i] = ld_stream_v4(x + r * cols + kb * 128 + lc * 8);
-  }
+  for (int i = 0; i < 4; ++i) v[i] = ld_stream_v4(xr + (4 * i + l4) * 8);
+  uint32_t m = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])), max(absmax_bits8(v[2]), absmax_bits8(v[3])));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  const bool fast = QuotientBracket::usable(sc);
+  const QuotientBracket qb(fast ? sc : 1.0f);
+  uint8_t* qr = q + r * cols + kb * 128;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int64_t r = rgrp * 64 + (t >> 4) + 16 * i;
-    uint32_t m = absmax_bits8(v[i]);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
     uint32_t p[4];
-    if (QuotientBracket::usable(sc)) {
-      const QuotientBracket qb(sc);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        p[j] = e4m3x2_quotient(bf16_bits_to_float(w[j] & 0xFFFFu), bf16_bits_to_float(w[j] >> 16), qb);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        p[j] = cvt_e4m3x2(__fdiv_rn(bf16_bits_to_float(w[j] & 0xFFFFu), sc),
-                          __fdiv_rn(bf16_bits_to_float(w[j] >> 16), sc));
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_bits_to_float(w[j] & 0xFFFFu), b = bf16_bits_to_float(w[j] >> 16);
+      p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
     }
-    *reinterpret_cast<uint2*>(q + r * cols + kb * 128 + lc * 8) = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-    if (lc == 0) s[kb * rows + r] = sc;
+    *reinterpret_cast<uint2*>(qr + (4 * i + l4) * 8) = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
   }
+  if (l4 == 0) s[kb * rows + r] = sc;
 }
 
 // DeepSeek 128x128 weight blocks: one CTA per block; 256 threads x 64 elements in registers.
@@ -388,14 +383,21 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
                                                              const unsigned int* __restrict__ amax_bits) {
   // grid: x = 32-row tile, y = 128-column tile; the last column tile may be half full
   // (cols % 128 == 64)
+  __shared__ float s_glob[2];  // s_g and rcp(s_g), computed once per CTA
   const int64_t tr = blockIdx.x, tc = blockIdx.y;
   const int t = threadIdx.x;
+  if (t == 0) {
+    const float amax = __uint_as_float(*amax_bits);
+    const float g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    s_glob[0] = g;
+    s_glob[1] = rcp_approx(g);
+    if (tr == 0 && tc == 0) *gscale = g;
+  }
+  __syncthreads();
+  const float sg = s_glob[0], rsg = s_glob[1];
   const int64_t r = tr * 32 + (t >> 3);
   const int64_t c = tc * 128 + (t & 7) * 16;
   if (c >= cols) return;
-  const float amax = __uint_as_float(*amax_bits);
-  const float sg = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
-  if (blockIdx.x == 0 && t == 0) *gscale = sg;
 
   const uint4 v0 = ld_stream_v4(x + r * cols + c);
   const uint4 v1 = ld_stream_v4(x + r * cols + c + 8);
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
   // t, so a +-2^-19 bracket that converts to one code decides it; otherwise the two IEEE quotients
   uint32_t scode;
   if (QuotientBracket::usable(sg)) {
-    const float y = __fmul_rn(__fmul_rn(bamax, 0.16666667163372040f), rcp_approx(sg));
+    const float y = __fmul_rn(__fmul_rn(bamax, 0.16666667163372040f), rsg);
     const uint32_t c0 = cvt_e4m3x2(__fmul_rn(y, kBracketDown), 0.0f) & 0xFFu;
     const uint32_t c1 = cvt_e4m3x2(__fmul_rn(y, kBracketUp), 0.0f) & 0xFFu;
     scode = (c0 == c1) ? c0 : (cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu);
