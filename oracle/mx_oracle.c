@@ -21,6 +21,7 @@
  *         blocks), sec 5.1 (worked tile), sec 6.3 (FP32 promotion every 128).
  *  [NV]   "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 2.4 (E2M1
  *         values), sec 3.2 (0.7 -> 0.5), sec 5.4 (two-level scale recipe),
+ *         sec 5.5 (MXFP4: E2M1 elements, 32-element blocks, one E8M0 scale),
  *         sec 5.6 (worked example), sec 7.1-7.4 (scale outside the sum, W4A4).
  *
  * Readings where the pages are silent (each is listed in the design doc):
@@ -33,7 +34,9 @@
  *  - The sign of zero is kept (-0 encodes as 0x80 / 0x8).
  *  - MX scale: k = floor(log2 amax) - emax, clamped to [-127, 127]; amax == 0
  *    gives k = -127.  A NaN or Inf anywhere in a block makes the block scale
- *    the E8M0 NaN code 0xFF and every code of that block 0x7F.
+ *    the E8M0 NaN code 0xFF and every code of that block 0x7F (E2M1 blocks of
+ *    MXFP4: 0x7, the largest positive code; the NaN scale already marks the
+ *    block, so these element codes are unpinned).
  *  - NVFP4: amax == 0 gives a global scale of 1.0; a block whose E4M3 scale
  *    code rounds to 0 gets all-zero element codes.  Element 2i is stored in the
  *    low nibble of byte i.
@@ -224,7 +227,7 @@ static void mx_block(const uint16_t* x, int64_t stride, int n, int fmt,
     }
     if (bad) {
         *s = 0xFF;
-        for (int i = 0; i < n; ++i) q[i * qstride] = 0x7F;
+        for (int i = 0; i < n; ++i) q[i * qstride] = (fmt == FMT_E2M1) ? 0x7 : 0x7F;
         return;
     }
     int k = orc_mx_scale_exp(amax, fmt);
@@ -236,7 +239,9 @@ static void mx_block(const uint16_t* x, int64_t stride, int n, int fmt,
 }
 
 /* row-wise: 1x32 blocks along each row.
-   x[rows][cols] bf16 -> q[rows][cols], s[rows][cols/32] (plain layout) */
+   x[rows][cols] bf16 -> q[rows][cols], s[rows][cols/32] (plain layout).
+   fmt E4M3 / E5M2 is MXFP8, E2M1 is MXFP4 ([NV] sec 5.5); codes are returned
+   one per byte (unpacked) for every format. */
 void orc_mx_quantize_rowwise(const uint16_t* x, int64_t rows, int64_t cols, int fmt,
                              uint8_t* q, uint8_t* s) {
     int64_t nb = cols / 32;
@@ -384,7 +389,8 @@ void orc_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols,
 /* listed in rows_idx (nrows of them).                                     */
 /* ---------------------------------------------------------------------- */
 
-/* MX: y = sum_b sA_b sB_b sum_{i<32} qA qB   ([MX] sec 0.3) */
+/* MX: y = sum_b sA_b sB_b sum_{i<32} qA qB   ([MX] sec 0.3); element formats
+   E4M3, E5M2 or E2M1 (MXFP4), codes one per byte */
 void orc_mx_gemm(const uint8_t* qa, const uint8_t* sa, int fa,
                  const uint8_t* qb, const uint8_t* sb, int fb,
                  int64_t M, int64_t N, int64_t K,
