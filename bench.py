@@ -9,6 +9,9 @@ One step = one pass over every row of the hot path, each on its own seeded synth
   nv   NVFP4 8192^3: two-pass quantize of A and B, block-scaled FP4 GEMM (FP32 out)
   ds   DeepSeek FP8 M=4096 K=7168 N=2048: 1x128 / 128x128 quantize, GEMM with FP32 promotion
        every 128 of K (bf16 out)
+An extra group, not part of the default step, is measured with --only mx4:
+  mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
+       with the block scales in the MMA (FP32 out)
 value = sum of GEMM FLOPs in the step / step time (TFLOP/s); per-row times, GB/s, TFLOP/s and
 roofline fractions are reported under "rows".  Every input exceeds or, within one step, is
 separated from its next use by far more than the 129 MB L2, so no explicit flush is needed.
@@ -39,6 +42,7 @@ WORKLOAD = "mxfp8_q16384x4096+mxfp8_linear_8192x4096x14336+nvfp4_8192^3+deepseek
 F_LIN = 2 * 8192 * 4096 * 14336            # each of fprop / dgrad / wgrad
 F_NV = 2 * 8192 ** 3
 F_DS = 2 * 4096 * 7168 * 2048
+F_MX4 = 2 * 8192 ** 3
 GEMM_FLOPS_STEP = 3 * F_LIN + F_NV + F_DS
 
 
@@ -60,6 +64,8 @@ Q2_BYTES = mx_q_bytes(16384, 4096, copies=4)
 LINQ_BYTES = mx_q_bytes(8192, 4096) + mx_q_bytes(14336, 4096) + mx_q_bytes(8192, 14336)
 NVQ_BYTES = 2 * nv_q_bytes(8192, 8192)
 DSQ_BYTES = ds_q_bytes(4096, 7168, 1) + ds_q_bytes(2048, 7168, 128)
+# MXFP4 row-wise: read bf16 + packed codes (1/2 B) + E8M0 scales (1/32 B), A and B
+MX4Q_BYTES = 2 * 8192 * 8192 * (2 + 0.5 + 1 / 32)
 
 
 def load_peaks():
@@ -134,7 +140,7 @@ class ClockSampler:
 class Workload:
     """All inputs and outputs of one step, resident on the device."""
 
-    GROUPS = ("q2", "lin", "nv", "ds")
+    GROUPS = ("q2", "lin", "nv", "ds")   # the default step; "mx4" only with --only
 
     def __init__(self, dev, groups=GROUPS):
         import torch
@@ -154,6 +160,8 @@ class Workload:
             self.host["A4"], self.host["B4"] = synthetic.nvfp4_pair()
         if "ds" in groups:
             self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
+        if "mx4" in groups:
+            self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
         self.d = {k: t(v) for k, v in self.host.items()}
         u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
         f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)
@@ -184,6 +192,12 @@ class Workload:
             self.Y5 = bf(4096, 2048)
             self.launches_per_step += 3
             self._outs += [self.Y5]
+        if "mx4" in groups:
+            self.A6q = (u8(8192, 4096), u8(sb(8192, 8192)))
+            self.B6q = (u8(8192, 4096), u8(sb(8192, 8192)))
+            self.Y6 = f32(8192, 8192)
+            self.launches_per_step += 3
+            self._outs += [self.Y6]
 
     def outputs(self):
         return list(self._outs)
@@ -225,10 +239,17 @@ class Workload:
             mark("dsgemm")
             mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
                                   out=self.Y5)
+        if "mx4" in g:
+            mark("mx4q")
+            for src, dst in ((d["A6"], self.A6q), (d["B6"], self.B6q)):
+                mx.mx_quantize(src, elem=mx.E2M1, layout=mx.ROWWISE, q_row=dst[0], s_row=dst[1])
+            mark("mx4gemm")
+            mx.mx_gemm(self.A6q[0], self.A6q[1], mx.E2M1, self.B6q[0], self.B6q[1], mx.E2M1, 8192, 8192, 8192,
+                       mx.OUT_F32, out=self.Y6)
         mark("end")
 
 
-ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm"]
+ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "mx4q", "mx4gemm"]
 
 
 def row_report(name, ms, peaks):
@@ -236,14 +257,14 @@ def row_report(name, ms, peaks):
     s = ms / 1e3
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (4.5 / 2.25 nominal)
     fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
-    if name in ("q2", "linq", "nvq", "dsq"):
-        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES}[name]
+    if name in ("q2", "linq", "nvq", "dsq", "mx4q"):
+        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES}[name]
         gbs = b / s / 1e9
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
-    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS}[name]
+    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4}[name]
     tf = f / s / 1e12
-    peak = fp4_peak if name == "nvgemm" else fp8_peak
+    peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
             "flops": int(f)}
 
@@ -420,7 +441,7 @@ def main():
     ap.add_argument("--library-reference", action="store_true",
                     help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
-                    help="comma-separated subset of row groups (q2, lin, nv, ds) for profiling runs; "
+                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4 is measured only here) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -499,17 +520,18 @@ def main():
     rows_ms = {n: v / args.steps for n, v in rows_ms.items()}
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
-    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS}
+    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
     kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
-               "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"]}
+               "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"],
+               "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
-                "ds_quantize": 2}
+                "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -518,14 +540,16 @@ def main():
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm"):
-        flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS}[dom]
-        peak = 3 * fp8_peak if dom == "nvfp4_gemm" else fp8_peak
+    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm"):
+        flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
+                 "mxfp4_gemm": F_MX4}[dom]
+        fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm")
+        peak = 3 * fp8_peak if fp4 else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
                 "per_launch": {"flops": flops // launches[dom], "avg_ms": round(dom_ms / launches[dom], 4)},
-                "peak_source": f"{peaks['source']}: bf16 sustained x {'6 (FP4)' if dom == 'nvfp4_gemm' else '2 (FP8)'}"
+                "peak_source": f"{peaks['source']}: bf16 sustained x {'6 (FP4)' if fp4 else '2 (FP8)'}"
                                " nominal dense ratio"}
     else:
         b = sum(rows[r]["bytes"] for r in kernels[dom])

@@ -147,12 +147,13 @@ def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int
             s_row = torch.empty(shape, dtype=torch.float32, device=dev)
     else:
         nb = mx_scale_bytes(rows, cols, block, block_rows, sfmt)
+        per_byte = 2 if elem == E2M1 else 1          # MXFP4 codes are packed two per byte
         if row and q_row is None:
-            q_row = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
+            q_row = torch.empty(rows, cols // per_byte, dtype=torch.uint8, device=dev)
         if row and s_row is None:
             s_row = _u8(nb, dev)
         if col and q_col is None:
-            q_col = torch.empty(cols, rows, dtype=torch.uint8, device=dev)
+            q_col = torch.empty(cols, rows // per_byte, dtype=torch.uint8, device=dev)
         if col and s_col is None:
             s_col = _u8(mx_scale_bytes(cols, rows, block, block_rows, sfmt), dev)
     st = load().mx_quantize(_ptr(x), rows, cols, block, block_rows, elem, sfmt, layout,
@@ -214,7 +215,8 @@ def _out(M, N, out_dtype, out, dev):
 
 
 def mx_gemm(qa, sa, ea, qb, sb, eb, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):
-    """C[m][n] = sum_b sA sB sum_i qA qB (MXFP8, include/mx.h mx_gemm)."""
+    """C[m][n] = sum_b sA sB sum_i qA qB (MXFP8, or MXFP4 with packed E2M1 codes; include/mx.h
+    mx_gemm)."""
     out, ldc = _out(M, N, out_dtype, out, qa.device)
     st = load().mx_gemm(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, M, N, K, out.data_ptr(), out_dtype, ldc,
                         _stream(stream))

@@ -158,7 +158,7 @@ template <int KIND, bool OUT_BF16>
 mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
   using Cfg = Gemm2Cfg<KIND>;
   static int max_clusters[64] = {};
-  const int64_t kc = (KIND == kMxf8) ? args.K / 128 : args.K / 64;
+  const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte scale chunks per 128 rows
   const int chunk_rows = Cfg::SF_CHUNK / 128;
   CUtensorMap ta, tb, tsa, tsb, tout;
   if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
@@ -193,6 +193,10 @@ mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int 
     if (row && col) MXQ(0, 1, true, true);
     else if (row) MXQ(0, 1, true, false);
     else MXQ(0, 1, false, true);
+  } else if (f0 == 2) {
+    if (row && col) MXQ(2, 1, true, true);
+    else if (row) MXQ(2, 1, true, false);
+    else MXQ(2, 1, false, true);
   } else {
     if (row && col) MXQ(1, 1, true, true);
     else if (row) MXQ(1, 1, true, false);
@@ -252,7 +256,7 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
   cudaStream_t st = as_stream(stream);
   const bool row = (layout & MX_ROWWISE) != 0, col = (layout & MX_COLWISE) != 0;
 
-  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0 && (elem == MX_E4M3 || elem == MX_E5M2)) {
+  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0) {  // MXFP8 (E4M3, E5M2) or MXFP4 (E2M1)
     if (row && (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 16))) return MX_ERR_INVALID_ARG;
     if (col && (!q_col || !s_col || !aligned(q_col, 16) || !aligned(s_col, 16))) return MX_ERR_INVALID_ARG;
     const int64_t tiles = (rows / 128) * (cols / 128);
@@ -262,7 +266,8 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     o.s_row[0] = static_cast<uint8_t*>(s_row);
     o.q_col[0] = static_cast<uint8_t*>(q_col);
     o.s_col[0] = static_cast<uint8_t*>(s_col);
-    return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, elem == MX_E4M3 ? 0 : 1, 1, row, col, o, st);
+    const int f0 = elem == MX_E4M3 ? 0 : (elem == MX_E5M2 ? 1 : 2);
+    return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, f0, 1, row, col, o, st);
   }
   if (block == 128 && sfmt == MX_SCALE_FP32 && elem == MX_E4M3 && layout == MX_ROWWISE &&
       (block_rows == 1 || block_rows == 128)) {
@@ -318,10 +323,13 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype)) return MX_ERR_INVALID_ARG;
   if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16))
     return MX_ERR_INVALID_ARG;
-  if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
-    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
-    return MX_ERR_INVALID_ARG;
+  const bool fp4 = ea == MX_E2M1 && eb == MX_E2M1;  // MXFP4 x MXFP4
+  if (!fp4) {
+    if ((ea != MX_E4M3 && ea != MX_E5M2 && ea != MX_E2M1) || (eb != MX_E4M3 && eb != MX_E5M2 && eb != MX_E2M1))
+      return MX_ERR_INVALID_ARG;
+    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;  // FP4 x FP8 mixes are not built
   }
+  if (fp4 && K % 256) return MX_ERR_INVALID_ARG;  // 256 FP4 elements of K per stage
   GemmArgs a{};
   a.sfa = static_cast<const uint8_t*>(sa);
   a.sfb = static_cast<const uint8_t*>(sb);
@@ -333,6 +341,16 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   const bool bn256 = (N % 256) == 0;
   cudaStream_t st = as_stream(stream);
   const bool bf = out_dtype == MX_OUT_BF16;
+  if (fp4) {  // kind::mxf4nvf4 operand type 1 = E2M1, UE8M0 scales; K / 2 bytes per row
+    const int64_t kb = K / 2;
+    if (bn256 && (M % 256) == 0) {
+      a.idesc = make_idesc_block_scaled(1u, 1u, 256, 256, 1);
+      return bf ? launch_gemm2<kMxf4, true>(qa, qb, kb, a, st) : launch_gemm2<kMxf4, false>(qa, qb, kb, a, st);
+    }
+    a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 1);
+    if (bn256) return bf ? launch_gemm<kMxf4, 256, true>(qa, qb, kb, a, st) : launch_gemm<kMxf4, 256, false>(qa, qb, kb, a, st);
+    return bf ? launch_gemm<kMxf4, 128, true>(qa, qb, kb, a, st) : launch_gemm<kMxf4, 128, false>(qa, qb, kb, a, st);
+  }
   if (bn256 && (M % 256) == 0) {
     a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
     return bf ? launch_gemm2<kMxf8, true>(qa, qb, K, a, st) : launch_gemm2<kMxf8, false>(qa, qb, K, a, st);

@@ -10,6 +10,9 @@
 //           "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 7.3 (four-step pipeline:
 //           narrow products, per-16 partial sums, times block scales, epilogue times the
 //           global scale) and sec 7.4 (scales of both operands).
+//   kMxf4 : MXFP4 -- kind::mxf4nvf4.block_scale.scale_vec::2X, E2M1 operands with one E8M0
+//           scale per 32 of K (the MX scale layout); "NVFP4: high accuracy with 4 bits"
+//           (theluyuan.com), sec 5.5.
 //   kDsF8 : DeepSeek FP8 -- kind::f8f6f4 over one 128-wide k-block at a time into one of four
 //           TMEM accumulators; epilogue warps promote every k-block into FP32 registers as
 //           acc += sA[kb][m] * sB[n/128][kb] * P while the tensor core fills the next buffers.
@@ -32,7 +35,12 @@
 
 namespace mxgb {
 
-enum GemmKind : int { kMxf8 = 0, kNvf4 = 1, kDsF8 = 2 };
+enum GemmKind : int { kMxf8 = 0, kNvf4 = 1, kDsF8 = 2, kMxf4 = 3 };
+
+// Bytes of scale chunks a stage needs per 128 rows: MX 1 chunk (128 of K), NVFP4 4 chunks (64 of
+// K each), MXFP4 2 chunks (256 of K); DeepSeek scales do not go through shared memory.
+constexpr int stage_sf_bytes(int kind) { return kind == kMxf8 ? 512 : (kind == kNvf4 ? 2048 : (kind == kMxf4 ? 1024 : 0)); }
+constexpr bool fp4_kind(int kind) { return kind == kNvf4 || kind == kMxf4; }
 
 constexpr int kSmemLimit = 232448;  // 227 KB opt-in dynamic shared memory per CTA
 
@@ -40,11 +48,11 @@ template <int KIND, int BN>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int KBYTES = 128;  // bytes of K per stage: one 128-byte swizzle row
-  static constexpr int K_ELEMS = (KIND == kNvf4) ? 256 : 128;
+  static constexpr int K_ELEMS = fp4_kind(KIND) ? 256 : 128;
   static constexpr int A_BYTES = BM * KBYTES;
   static constexpr int B_BYTES = BN * KBYTES;
   static constexpr int RC = BN / 128;  // 128-row scale chunks of B per tile
-  static constexpr int SFA_BYTES = (KIND == kMxf8) ? 512 : (KIND == kNvf4 ? 2048 : 0);
+  static constexpr int SFA_BYTES = stage_sf_bytes(KIND);
   static constexpr int SFB_BYTES = SFA_BYTES * RC;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int BAR_BYTES = 1024;
@@ -58,8 +66,8 @@ struct GemmCfg {
   static constexpr int ACC_COLS = NBUF * BN;
   // Scale factors get their own TMEM columns per pipeline stage, so the tcgen05.cp of stage s+1
   // carries no write-after-read dependency on the MMAs still reading stage s's scales.
-  static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : (KIND == kNvf4 ? 16 : 0);
-  static constexpr int SFB_COLS = (KIND == kMxf8) ? 4 * RC : (KIND == kNvf4 ? 16 * RC : 0);
+  static constexpr int SFA_COLS = SFA_BYTES / 128;  // one 512-byte chunk fills 4 columns
+  static constexpr int SFB_COLS = SFA_COLS * RC;
   static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;
   static constexpr int SFA_COL = ACC_COLS;             // + stage * SF_STAGE_COLS
   static constexpr int SFB_COL = ACC_COLS + SFA_COLS;  // + stage * SF_STAGE_COLS
@@ -205,6 +213,14 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
               bulk_load(sSFB + stage * Cfg::SFB_BYTES + rc * 512,
                         args.sfb + ((static_cast<int64_t>(nb) * Cfg::RC + rc) * kchunks_mx + kt) * 512, 512,
                         &full_bar[stage]);
+          } else if (KIND == kMxf4) {  // MX chunks 2kt, 2kt + 1: 1 KB per 128 rows
+            bulk_load(sSFA + stage * Cfg::SFA_BYTES, args.sfa + (mb * kchunks_mx + 2ll * kt) * 512, 1024,
+                      &full_bar[stage]);
+#pragma unroll
+            for (int rc = 0; rc < Cfg::RC; ++rc)
+              bulk_load(sSFB + stage * Cfg::SFB_BYTES + rc * 1024,
+                        args.sfb + ((static_cast<int64_t>(nb) * Cfg::RC + rc) * kchunks_mx + 2ll * kt) * 512, 1024,
+                        &full_bar[stage]);
           } else if (KIND == kNvf4) {
             bulk_load(sSFA + stage * Cfg::SFA_BYTES, args.sfa + (mb * kchunks_nv + 4ll * kt) * 512, 2048,
                       &full_bar[stage]);
@@ -277,6 +293,9 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
             if (KIND == kMxf8) {
               umma_mxf8f6f4(d_tmem, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), sfa_t, sfb_t,
                             (kt > 0 || j > 0) ? 1u : 0u);
+            } else if (KIND == kMxf4) {  // MMA j: scale chunk j / 2, bytes 2 (j % 2) .. + 1 of each row
+              umma_mxf4(d_tmem, adesc, bdesc, idesc_with_sf_ids(args.idesc, 2 * (j & 1), 2 * (j & 1)),
+                        sfa_t + 4 * (j >> 1), sfb_t + (j >> 1) * 4 * Cfg::RC, (kt > 0 || j > 0) ? 1u : 0u);
             } else if (KIND == kNvf4) {
               umma_mxf4nvf4(d_tmem, adesc, bdesc, args.idesc, sfa_t + 4 * j, sfb_t + j * 4 * Cfg::RC,
                             (kt > 0 || j > 0) ? 1u : 0u);
@@ -328,13 +347,15 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
             for (int rc = 0; rc < Cfg::RC; ++rc)
               tmem_cp_32x128b_warpx4(sfb_t + 4 * rc, desc_from_words(sfb_lo + rc * (512 >> 4), kSfHi));
           } else {
+            // chunk c of A's scales -> columns 4c; chunk c of B's row block rc -> 4 (c RC + rc)
+            constexpr int NCH = Cfg::SFA_BYTES / 512;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tmem_cp_32x128b_warpx4(sfa_t + 4 * j, desc_from_words(sfa_lo + j * (512 >> 4), kSfHi));
+            for (int c = 0; c < NCH; ++c) {
+              tmem_cp_32x128b_warpx4(sfa_t + 4 * c, desc_from_words(sfa_lo + c * (512 >> 4), kSfHi));
 #pragma unroll
               for (int rc = 0; rc < Cfg::RC; ++rc)
-                tmem_cp_32x128b_warpx4(sfb_t + j * 4 * Cfg::RC + 4 * rc,
-                                       desc_from_words(sfb_lo + ((rc * 2048 + j * 512) >> 4), kSfHi));
+                tmem_cp_32x128b_warpx4(sfb_t + c * 4 * Cfg::RC + 4 * rc,
+                                       desc_from_words(sfb_lo + ((rc * Cfg::SFA_BYTES + c * 512) >> 4), kSfHi));
             }
           }
           umma_commit(&sfready_bar[stage]);

@@ -1,7 +1,8 @@
 // mx_gemm2.cuh -- block-scaled GEMMs on CTA pairs (tcgen05 cta_group::2) for sm_103a.
 //
-// Same products as the single-CTA kernel (kMxf8: MXFP8 with E8M0 scales per 32 of K; kNvf4:
-// NVFP4 with E4M3 scales per 16 and FP32 global scales in the epilogue), but one 256 x 256 output
+// Same products as the single-CTA kernel (kMxf8: MXFP8 with E8M0 scales per 32 of K; kMxf4:
+// MXFP4, E2M1 with E8M0 scales per 32; kNvf4: NVFP4 with E4M3 scales per 16 and FP32 global
+// scales in the epilogue), but one 256 x 256 output
 // tile is computed by a cluster of two CTAs on two SMs with M = 256 tcgen05.mma instructions:
 //   * each CTA loads its own 128 rows of A and its own 128 rows (half) of B per stage; the pair's
 //     MMA reads both halves of B, so every SM receives 2/3 of the operand bytes the single-CTA
@@ -64,10 +65,10 @@ struct Gemm2Cfg {
   static constexpr int BN = 256;       // columns per pair tile
   static constexpr int ROWS = 128;     // A rows and B rows each CTA loads
   static constexpr int KBYTES = 128;   // bytes of K per stage
-  static constexpr int K_ELEMS = (KIND == kNvf4) ? 256 : 128;
+  static constexpr int K_ELEMS = fp4_kind(KIND) ? 256 : 128;
   static constexpr int A_BYTES = ROWS * KBYTES;
   static constexpr int B_BYTES = ROWS * KBYTES;
-  static constexpr int SF_CHUNK = (KIND == kMxf8) ? 512 : 2048;  // scale bytes per 128 rows per stage
+  static constexpr int SF_CHUNK = stage_sf_bytes(KIND);  // scale bytes per 128 rows per stage
   static constexpr int SFA_BYTES = SF_CHUNK;       // own 128 rows of A
   static constexpr int SFB_BYTES = 2 * SF_CHUNK;   // all 256 rows of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -80,8 +81,8 @@ struct Gemm2Cfg {
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING + BAR_BYTES;
   static constexpr int NUM_MMA = KBYTES / 32;
   static constexpr int ACC_COLS = BN;
-  static constexpr int SFA_COLS = (KIND == kMxf8) ? 4 : 16;
-  static constexpr int SFB_COLS = (KIND == kMxf8) ? 8 : 32;
+  static constexpr int SFA_COLS = SF_CHUNK / 128;  // a 512-byte chunk fills 4 TMEM columns
+  static constexpr int SFB_COLS = 2 * SFA_COLS;
   static constexpr int SF_STAGE_COLS = SFA_COLS + SFB_COLS;  // each stage has its own scale columns
   static constexpr int SFA_COL = ACC_COLS;                     // + stage * SF_STAGE_COLS
   static constexpr int SFB_COL = ACC_COLS + SFA_COLS;          // + stage * SF_STAGE_COLS
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
-      const int64_t kc = (KIND == kMxf8) ? args.K / 128 : args.K / 64;  // 512-byte chunks per 128 rows
+      const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte chunks per 128 rows
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
         int mb, nb;
@@ -185,8 +186,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
           tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmA, full_leader, kt * Cfg::KBYTES, a_row);
           tma_load_2d_pair(sB + stage * Cfg::B_BYTES, &tmB, full_leader, kt * Cfg::KBYTES, b_row);
           // 512-byte scale chunk (rb, c) starts at 128-byte row (rb * kc + c) * 4; a stage needs
-          // chunk c = kt (MX) or chunks 4kt .. 4kt+3 (NVFP4, contiguous; one 2 KB box)
-          const int64_t cfirst = (KIND == kMxf8) ? kt : 4ll * kt;
+          // chunk c = kt (MXFP8), chunks 2kt, 2kt+1 (MXFP4) or 4kt .. 4kt+3 (NVFP4), contiguous,
+          // so one box
+          const int64_t cfirst = static_cast<int64_t>(Cfg::SF_CHUNK / 512) * kt;
           tma_load_2d_pair(sSFA + stage * Cfg::SFA_BYTES, &tmSFA, full_leader, 0,
                            static_cast<int32_t>(((a_row / 128) * kc + cfirst) * 4));
 #pragma unroll
@@ -245,6 +247,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
             const uint32_t acc = (kt > 0 || j > 0) ? 1u : 0u;
             if (KIND == kMxf8)
               umma_mxf8f6f4_pair(tmem_base, adesc, bdesc, idesc_with_sf_ids(args.idesc, j, j), sfa_t, sfb_t, acc);
+            else if (KIND == kMxf4)  // MMA j: scale chunk j / 2, bytes 2 (j % 2) .. + 1 of each row
+              umma_mxf4_pair(tmem_base, adesc, bdesc, idesc_with_sf_ids(args.idesc, 2 * (j & 1), 2 * (j & 1)),
+                             sfa_t + 4 * (j >> 1), sfb_t + 8 * (j >> 1), acc);
             else
               umma_mxf4nvf4_pair(tmem_base, adesc, bdesc, args.idesc, sfa_t + 4 * j, sfb_t + 8 * j, acc);
           }
@@ -284,9 +289,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
           const uint32_t sfb_lo = sfb_lo0 + stage * (Cfg::SFB_BYTES >> 4);
           const uint32_t sfa_t = tmem_base + Cfg::SFA_COL + stage * Cfg::SF_STAGE_COLS;
           const uint32_t sfb_t = tmem_base + Cfg::SFB_COL + stage * Cfg::SF_STAGE_COLS;
-          // an MXFP8 stage's one MMA group reads one chunk of each scale tensor (its four MMAs
-          // pick bytes with the scale ids); an NVFP4 stage has a chunk per MMA
-          constexpr int NCOPY = (KIND == kMxf8) ? 3 : 3 * Cfg::NUM_MMA;
+          // an MXFP8 stage's four MMAs read one chunk of each scale tensor (bytes picked by the
+          // scale ids), an MXFP4 stage's read two (one per pair of MMAs), an NVFP4 stage's four
+          constexpr int NCOPY = 3 * (Cfg::SF_CHUNK / 512);
 #pragma unroll
           for (int c = 0; c < NCOPY; ++c) {
             if (c % Cfg::SF_ISSUERS != part) continue;

@@ -46,6 +46,13 @@ struct MxElem<1> {
   static constexpr int emax = 15;
   __device__ static uint32_t cvt2(float lo, float hi) { return cvt_e5m2x2(lo, hi); }
 };
+// MXFP4: E2M1 elements (largest value 6 = 1.5 * 2^2), two codes per byte, element 2i in the low
+// nibble.  "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 5.5.
+template <>
+struct MxElem<2> {
+  static constexpr int emax = 2;
+  __device__ static uint32_t cvt2(float lo, float hi) { return cvt_e2m1x2(lo, hi); }
+};
 
 // E8M0 scale byte from the largest |x| bit pattern (bf16 bits & 0x7fff) of a finite block:
 // k = floor(log2 amax) - emax clamped to >= -127; byte = k + 127 = max(expfield - emax, 0).
@@ -71,6 +78,19 @@ __device__ __forceinline__ uint2 mx_codes8(uint4 v, float inv) {
     p[i] = MxElem<ELEM>::cvt2(lo, hi);
   }
   return make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+}
+
+// Quantize 8 bf16 values to E2M1 with inverse scale `inv`; returns 4 bytes of packed codes.
+__device__ __forceinline__ uint32_t mx_codes8_e2m1(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t p = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __fmul_rn(bf16_bits_to_float(w[i] & 0xFFFFu), inv);
+    const float hi = __fmul_rn(bf16_bits_to_float(w[i] >> 16), inv);
+    p |= cvt_e2m1x2(lo, hi) << (8 * i);
+  }
+  return p;
 }
 
 // largest |x| bit pattern (bf16 bits with the sign cleared) of 8 bf16 values; the two halves of
@@ -175,6 +195,18 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
       uint32_t m = absmax_bits8(v[i]);
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
       m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      if constexpr (F0 == 2) {  // MXFP4: packed E2M1, a NaN or Inf block gets codes 0x7
+        uint32_t packed, sbyte;
+        if (m >= 0x7F80u) {
+          sbyte = 0xFF;
+          packed = 0x77777777u;
+        } else {
+          sbyte = mx_scale_byte<2>(m);
+          packed = mx_codes8_e2m1(v[i], mx_inv_scale(sbyte));
+        }
+        *reinterpret_cast<uint32_t*>(o.q_row[0] + (tr * 128 + r) * (cols >> 1) + tc * 64 + lc * 4) = packed;
+        if ((lc & 3) == 0) srow[0][chunk_offset(r, lc >> 2)] = static_cast<uint8_t>(sbyte);
+      } else {
 #pragma unroll
       for (int f = 0; f < NF; ++f) {
         uint2 codes;
@@ -191,6 +223,7 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
         }
         *reinterpret_cast<uint2*>(o.q_row[f] + (tr * 128 + r) * cols + tc * 128 + lc * 8) = codes;
         if ((lc & 3) == 0) srow[f][chunk_offset(r, lc >> 2)] = static_cast<uint8_t>(sbyte);
+      }
       }
     }
   }
@@ -216,6 +249,38 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) m[j] = max(m[j], __shfl_xor_sync(0xFFFFFFFFu, m[j], 1));
+    if constexpr (F0 == 2) {  // MXFP4: 16 codes per column -> 8 bytes
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * cq + j;
+        uint32_t w2[2], sbyte;
+        if (m[j] >= 0x7F80u) {
+          sbyte = 0xFF;
+          w2[0] = w2[1] = 0x77777777u;
+        } else {
+          sbyte = mx_scale_byte<2>(m[j]);
+          const float inv = mx_inv_scale(sbyte);
+          const int sh = (j & 1) ? 16 : 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // rows 8h + 2k, 8h + 2k + 1 -> byte k
+              const int ra = 8 * h + 2 * k;
+              const uint32_t ea = ((j < 2) ? u[ra].x : u[ra].y) >> sh;
+              const uint32_t eb = ((j < 2) ? u[ra + 1].x : u[ra + 1].y) >> sh;
+              const float fa = __fmul_rn(bf16_bits_to_float(ea & 0xFFFFu), inv);
+              const float fb = __fmul_rn(bf16_bits_to_float(eb & 0xFFFFu), inv);
+              acc |= cvt_e2m1x2(fa, fb) << (8 * k);
+            }
+            w2[h] = acc;
+          }
+        }
+        uint8_t* dst = o.q_col[0] + (tc * 128 + c) * (rows >> 1) + tr * 64 + rb * 16 + hb * 8;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w2[0], w2[1]);
+        if (hb == 0) scol[0][chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
+      }
+    } else {
 #pragma unroll
     for (int f = 0; f < NF; ++f) {
 #pragma unroll
@@ -248,6 +313,7 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
         *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         if (hb == 0) scol[f][chunk_offset(c, rb)] = static_cast<uint8_t>(sbyte);
       }
+    }
     }
   }
 

@@ -20,6 +20,7 @@ WORKLOADS = {
     "mxfp8_linear_8192x4096x14336": "MXFP8 linear layer M=8192 K=4096 N=14336: fprop, dgrad, wgrad",
     "nvfp4_8192": "NVFP4 quantize + GEMM 8192^3, N(0,1) with 0.1% outliers at 50x",
     "deepseek_fp8_4096x7168x2048": "DeepSeek FP8 GEMM M=4096 K=7168 N=2048, 1x128 / 128x128 FP32 scales",
+    "mxfp4_8192": "MXFP4 quantize + GEMM 8192^3, N(0,1) with 0.1% outliers at 50x",
 }
 
 OUTLIER_COLS_4096 = (5, 1029, 2058, 3087)
@@ -92,6 +93,11 @@ def nvfp4_pair(M=8192, N=8192, K=8192):
     a = with_sparse_outliers(M, K, 4000)
     b = with_sparse_outliers(N, K, 4001)
     return a, b
+
+
+def mxfp4_pair(M=8192, N=8192, K=8192):
+    """MXFP4 product operands: the NVFP4 recipe (N(0,1) with 0.1% of elements x50), own seeds."""
+    return with_sparse_outliers(M, K, 6000), with_sparse_outliers(N, K, 6001)
 
 
 def deepseek_pair(M=4096, N=2048, K=7168):

@@ -81,15 +81,18 @@ const char* mx_status_string(mx_status s);
  * axis of the consuming GEMM) for the row-wise copy and along rows for the column-wise copy.
  *
  * Supported combinations (anything else returns MX_ERR_UNSUPPORTED):
- *  1. MX: block = 32, block_rows = 1, elem = MX_E4M3 or MX_E5M2, sfmt = MX_SCALE_E8M0,
- *     layout = ROWWISE, COLWISE or BOTH; rows % 128 == 0, cols % 128 == 0.
+ *  1. MX: block = 32, block_rows = 1, elem = MX_E4M3 or MX_E5M2 (MXFP8) or MX_E2M1
+ *     (MXFP4, [NV] sec 5.5), sfmt = MX_SCALE_E8M0, layout = ROWWISE, COLWISE or BOTH;
+ *     rows % 128 == 0, cols % 128 == 0.
  *     Per block: amax = max |x|; k = clamp(floor(log2 amax) - emax, -127, 127) with emax 8
- *     (E4M3) or 15 (E5M2), k = -127 when amax == 0; scale byte = k + 127;
+ *     (E4M3), 15 (E5M2) or 2 (E2M1), k = -127 when amax == 0; scale byte = k + 127;
  *     q = RNE-satfinite(x * 2^-k).  A NaN or Inf in a block gives scale 0xFF and all codes
- *     0x7F.  With BOTH, both copies come from one read of x.
+ *     0x7F (E2M1: 0x7).  With BOTH, both copies come from one read of x.
  *       q_row[rows][cols] u8, s_row: rows*cols/32 bytes in the MX GEMM layout;
  *       q_col[cols][rows] u8 (transposed), s_col: the MX GEMM layout of that [cols][rows]
  *       matrix.  Pointers of a copy that is not requested may be NULL.
+ *       MXFP4 codes are packed two per byte, element 2i in the low nibble:
+ *       q_row[rows][cols/2], q_col[cols][rows/2].
  *  2. DeepSeek activations: block = 128, block_rows = 1, elem = MX_E4M3,
  *     sfmt = MX_SCALE_FP32, layout = ROWWISE; rows % 128 == 0, cols % 128 == 0.
  *     s = fl32(amax / 448) (1.0 when amax == 0); q = RNE-satfinite(fl32(x / s)).
@@ -116,12 +119,15 @@ mx_status mx_quantize_dual(const void* x, int64_t rows, int64_t cols, mx_layout 
                            void* stream);
 
 /*
- * mx_gemm -- MXFP8 block-scaled GEMM.  [MX] sec 0.3:
+ * mx_gemm -- MX block-scaled GEMM (MXFP8, MXFP4).  [MX] sec 0.3, [NV] sec 5.5:
  *   C[m][n] = sum_b sA[m][b] sB[n][b] sum_{i<32} qA[m][32b+i] qB[n][32b+i], FP32 accumulate.
  *
  * qa[M][K], qb[N][K]: E4M3 or E5M2 codes (ea, eb), 16-byte aligned; sa, sb: E8M0 scales in
  * the MX GEMM layout.  out: M rows of ldc elements (ldc >= N, ldc % 8 == 0), FP32 or bf16
  * (RNE).  M % 128 == 0, N % 128 == 0, K % 128 == 0.
+ * MXFP4: ea = eb = MX_E2M1, qa[M][K/2], qb[N][K/2] packed (element 2i in the low nibble, as
+ * mx_quantize writes them), K % 256 == 0.  An E2M1 operand with an FP8 one returns
+ * MX_ERR_UNSUPPORTED.
  */
 mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea,
                   const void* qb, const void* sb, mx_elem eb,

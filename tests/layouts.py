@@ -24,3 +24,9 @@ def unpack_fp4(qp):
     """packed [rows][cols/2] -> codes [rows][cols] (element 2i in the low nibble)."""
     qp = np.asarray(qp)
     return np.stack([qp & 0xF, qp >> 4], axis=-1).reshape(qp.shape[0], -1)
+
+
+def pack_fp4(codes):
+    """codes [rows][cols] (4-bit values) -> packed [rows][cols/2], element 2i in the low nibble."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.ascontiguousarray(c[:, 0::2] | (c[:, 1::2] << 4))

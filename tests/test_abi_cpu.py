@@ -74,7 +74,7 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(qc=None) == mx.MX_ERR_INVALID_ARG          # column-wise requested, no buffer
     assert call(block=64) == mx.MX_ERR_UNSUPPORTED
     assert call(block=128, sfmt=2, layout=2) == mx.MX_ERR_UNSUPPORTED   # DeepSeek column-wise
-    assert call(elem=2) == mx.MX_ERR_UNSUPPORTED            # E2M1 with E8M0 (MXFP4) not built
+    assert call(elem=2, block=16) == mx.MX_ERR_UNSUPPORTED  # E2M1 blocks of 16 with E8M0: not MX
     assert call(rows=128, cols=65536 * 128) == mx.MX_ERR_INVALID_ARG   # more than 65535 column tiles
 
 
@@ -100,7 +100,9 @@ def test_gemms_reject_bad_arguments(lib):
     assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 96, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG
     assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 64, None) == mx.MX_ERR_INVALID_ARG
     assert g(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 128, 128, FAKE, 5, 128, None) == mx.MX_ERR_INVALID_ARG
-    assert g(FAKE, FAKE, 2, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_UNSUPPORTED
+    assert g(FAKE, FAKE, 2, FAKE, FAKE, 0, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_UNSUPPORTED  # FP4 x FP8
+    assert g(FAKE, FAKE, 2, FAKE, FAKE, 2, 128, 128, 128, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG  # MXFP4 K % 256
+    assert g(FAKE, FAKE, 7, FAKE, FAKE, 2, 128, 128, 256, FAKE, 1, 128, None) == mx.MX_ERR_INVALID_ARG  # bad enum
     n = lib.nvfp4_gemm
     assert n(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 128, FAKE, 0, 128, None) == mx.MX_ERR_INVALID_ARG
     assert n(FAKE, FAKE, None, FAKE, FAKE, FAKE, 128, 128, 256, FAKE, 0, 128, None) == mx.MX_ERR_INVALID_ARG

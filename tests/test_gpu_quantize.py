@@ -16,7 +16,7 @@ from tests.layouts import chunked_to_plain
 
 pytestmark = pytest.mark.gpu
 
-EMAX = {orc.E4M3: 8, orc.E5M2: 15}
+EMAX = {orc.E4M3: 8, orc.E5M2: 15, orc.E2M1: 2}
 MXFMT = {orc.E4M3: mx.E4M3, orc.E5M2: mx.E5M2}
 
 
