@@ -70,6 +70,12 @@ def _load():
                 "orc_nv_gemm": (None, [p, p, f32, p, p, f32, i64, i64, i64, p, i64, p, p]),
                 "orc_ds_gemm": (None, [p, p, p, p, i64, i64, i64, p, i64, p, p]),
                 "orc_num_threads": (i32, []),
+                "orc_pow2_scale_exp": (i32, [f64]),
+                "orc_ds_quantize_1x128_pow2": (None, [p, i64, i64, p, p]),
+                "orc_ds_quantize_128x128_pow2": (None, [p, i64, i64, p, p]),
+                "orc_e8m0_of_scale": (ctypes.c_uint8, [f32]),
+                "orc_mx_scales_from_blocks": (None, [p, i64, i64, i32, p]),
+                "orc_mx_quantize_2d32": (None, [p, i64, i64, i32, p, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -167,6 +173,54 @@ def ds_quantize_128x128(x):
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows // 128, cols // 128), np.float32)
     _load().orc_ds_quantize_128x128(_ptr(xb), rows, cols, _ptr(q), _ptr(s))
+    return q, s
+
+
+# ---------------------------------------------------------------- power-of-two blocks, 2-D MX
+def pow2_scale_exp(amax: float) -> int:
+    return _load().orc_pow2_scale_exp(amax)
+
+
+def ds_quantize_1x128_pow2(x):
+    """1x128 tiles, power-of-two FP32 scales: (q [rows][cols], s [rows][cols/128])."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 128), np.float32)
+    _load().orc_ds_quantize_1x128_pow2(_ptr(xb), rows, cols, _ptr(q), _ptr(s))
+    return q, s
+
+
+def ds_quantize_128x128_pow2(x):
+    """128x128 blocks, power-of-two FP32 scales: (q [rows][cols], s [rows/128][cols/128])."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows // 128, cols // 128), np.float32)
+    _load().orc_ds_quantize_128x128_pow2(_ptr(xb), rows, cols, _ptr(q), _ptr(s))
+    return q, s
+
+
+def e8m0_of_scale(sc: float) -> int:
+    return _load().orc_e8m0_of_scale(sc)
+
+
+def mx_scales_from_blocks(s, rows: int, cols: int, block_rows: int):
+    """Per-32 E8M0 codes [rows][cols/32] from 1x128 (s [rows][cols/128]) or 128x128
+    (s [rows/128][cols/128]) power-of-two FP32 block scales; 0xFF where a scale is not 2^k."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    out = np.empty((rows, cols // 32), np.uint8)
+    _load().orc_mx_scales_from_blocks(_ptr(s), rows, cols, block_rows, _ptr(out))
+    return out
+
+
+def mx_quantize_2d32(x, fmt: int):
+    """2-D 32x32 MX blocks: (q [rows][cols], s [rows/32][cols/32])."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows // 32, cols // 32), np.uint8)
+    _load().orc_mx_quantize_2d32(_ptr(xb), rows, cols, fmt, _ptr(q), _ptr(s))
     return q, s
 
 

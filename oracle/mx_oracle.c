@@ -322,6 +322,120 @@ void orc_ds_quantize_128x128(const uint16_t* x, int64_t rows, int64_t cols,
 }
 
 /* ---------------------------------------------------------------------- */
+/* Float8BlockScaling with power-of-two scales and its MX form, [MX] sec  */
+/* 1.3: on Blackwell the 1x128 / 128x128 recipe's FP32 scales are powers   */
+/* of two, so each converts to an E8M0 code; a 128-block's scale serves    */
+/* its four 32-blocks unchanged and a 2-D block's scale is broadcast to    */
+/* every row; the FP8 codes are reused as they are.                        */
+/* Reading (the page does not give the rounding of the scale): s = 2^k,    */
+/* k the smallest integer with 448 * 2^k >= amax (no element saturates),   */
+/* clamped to [-127, 127]; amax == 0 gives s = 1.  q = E4M3(x / s), exact. */
+/* ---------------------------------------------------------------------- */
+int orc_pow2_scale_exp(double amax) {
+    if (amax == 0.0) return 0;
+    int k = -127;
+    while (k < 127 && ldexp(448.0, k) < amax) ++k;   /* linear search, no shortcuts */
+    return k;
+}
+
+/* 1x128 tiles with power-of-two scales: q[rows][cols], s[rows][cols/128] (plain) */
+void orc_ds_quantize_1x128_pow2(const uint16_t* x, int64_t rows, int64_t cols,
+                                uint8_t* q, float* s) {
+    int64_t nb = cols / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            double amax = 0.0;
+            for (int i = 0; i < 128; ++i) {
+                double a = fabs(orc_bf16(x[r * cols + b * 128 + i]));
+                if (a > amax) amax = a;
+            }
+            int k = orc_pow2_scale_exp(amax);
+            s[r * nb + b] = (float)ldexp(1.0, k);
+            for (int i = 0; i < 128; ++i)
+                q[r * cols + b * 128 + i] =
+                    (uint8_t)orc_encode(FMT_E4M3, ldexp(orc_bf16(x[r * cols + b * 128 + i]), -k));
+        }
+}
+
+/* 128x128 blocks with power-of-two scales: q[rows][cols], s[rows/128][cols/128] */
+void orc_ds_quantize_128x128_pow2(const uint16_t* x, int64_t rows, int64_t cols,
+                                  uint8_t* q, float* s) {
+    int64_t nbr = rows / 128, nbc = cols / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t br = 0; br < nbr; ++br)
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            double amax = 0.0;
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    double a = fabs(orc_bf16(x[(br * 128 + i) * cols + bc * 128 + j]));
+                    if (a > amax) amax = a;
+                }
+            int k = orc_pow2_scale_exp(amax);
+            s[br * nbc + bc] = (float)ldexp(1.0, k);
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    int64_t o = (br * 128 + i) * cols + bc * 128 + j;
+                    q[o] = (uint8_t)orc_encode(FMT_E4M3, ldexp(orc_bf16(x[o]), -k));
+                }
+        }
+}
+
+/* E8M0 code of an FP32 scale: k + 127 when the scale is exactly 2^k with
+   -127 <= k <= 127, otherwise the E8M0 NaN code 0xFF */
+uint8_t orc_e8m0_of_scale(float sc) {
+    double v = (double)sc;
+    if (!(v > 0.0) || isinf(v)) return 0xFF;
+    int e; double m = frexp(v, &e);              /* v = m 2^e, m in [0.5, 1) */
+    if (m != 0.5) return 0xFF;
+    int k = e - 1;
+    if (k < -127 || k > 127) return 0xFF;
+    return (uint8_t)(k + 127);
+}
+
+/* Expand block scales into per-32 MX scales of the [rows][cols] code matrix:
+   block_rows 1:   s[rows][cols/128] (1x128 tiles),
+   block_rows 128: s[rows/128][cols/128] (128x128 blocks);
+   out[rows][cols/32] E8M0 codes (plain layout). */
+void orc_mx_scales_from_blocks(const float* s, int64_t rows, int64_t cols, int block_rows,
+                               uint8_t* out) {
+    int64_t nb = cols / 32, nbc = cols / 128;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            float sc = (block_rows == 1) ? s[r * nbc + b / 4] : s[(r / 128) * nbc + b / 4];
+            out[r * nb + b] = orc_e8m0_of_scale(sc);
+        }
+}
+
+/* 2-D 32x32 MX blocks ([MX] sec 1.3): one E8M0 scale per 32x32 block by the
+   MX rule over the whole block; codes q[rows][cols]; scales s[rows/32][cols/32].
+   The row-wise MX form uses s[r/32][b] for row r, block b; the column-wise
+   (transposed) form is the transpose of q with s[b][c/32]. */
+void orc_mx_quantize_2d32(const uint16_t* x, int64_t rows, int64_t cols, int fmt,
+                          uint8_t* q, uint8_t* s) {
+    int64_t nbr = rows / 32, nbc = cols / 32;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t br = 0; br < nbr; ++br)
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            double amax = 0.0; int bad = 0;
+            for (int i = 0; i < 32; ++i)
+                for (int j = 0; j < 32; ++j) {
+                    double v = orc_bf16(x[(br * 32 + i) * cols + bc * 32 + j]);
+                    if (!isfinite(v)) bad = 1;
+                    else if (fabs(v) > amax) amax = fabs(v);
+                }
+            int k = orc_mx_scale_exp(amax, fmt);
+            s[br * nbc + bc] = bad ? 0xFF : (uint8_t)(k + 127);
+            for (int i = 0; i < 32; ++i)
+                for (int j = 0; j < 32; ++j) {
+                    int64_t o = (br * 32 + i) * cols + bc * 32 + j;
+                    q[o] = bad ? (uint8_t)((fmt == FMT_E2M1) ? 0x7 : 0x7F)
+                               : (uint8_t)orc_encode(fmt, ldexp(orc_bf16(x[o]), -k));
+                }
+        }
+}
+
+/* ---------------------------------------------------------------------- */
 /* NVFP4 two-level quantization, [NV] sec 5.4 and 5.6                     */
 /* ---------------------------------------------------------------------- */
 float orc_nv_global_scale(float amax) {
