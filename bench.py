@@ -12,6 +12,9 @@ One step = one pass over every row of the hot path, each on its own seeded synth
 An extra group, not part of the default step, is measured with --only mx4:
   mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
        with the block scales in the MMA (FP32 out)
+  blk  Float8BlockScaling through the MX GEMM at the DeepSeek shape (M=4096 K=7168 N=2048):
+       power-of-two 1x128 / 128x128 quantize, scale conversion to E8M0, MXFP8 GEMM (bf16 out);
+       and 2-D 32x32 MX quantize of the 14336x4096 weight (row- and column-wise)
 value = sum of GEMM FLOPs in the step / step time (TFLOP/s); per-row times, GB/s, TFLOP/s and
 roofline fractions are reported under "rows".  Every input exceeds or, within one step, is
 separated from its next use by far more than the 129 MB L2, so no explicit flush is needed.
@@ -66,6 +69,9 @@ NVQ_BYTES = 2 * nv_q_bytes(8192, 8192)
 DSQ_BYTES = ds_q_bytes(4096, 7168, 1) + ds_q_bytes(2048, 7168, 128)
 # MXFP4 row-wise: read bf16 + packed codes (1/2 B) + E8M0 scales (1/32 B), A and B
 MX4Q_BYTES = 2 * 8192 * 8192 * (2 + 0.5 + 1 / 32)
+# scale conversion: read the FP32 block scales, write one E8M0 byte per 32 elements
+BLKCONV_BYTES = 4 * 4096 * 56 + 4 * 16 * 56 + (4096 + 2048) * 7168 // 32
+W2DQ_BYTES = mx_q_bytes(14336, 4096)
 
 
 def load_peaks():
@@ -162,6 +168,9 @@ class Workload:
             self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
         if "mx4" in groups:
             self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
+        if "blk" in groups:
+            self.host["A7"], self.host["B7"] = synthetic.deepseek_pair()
+            self.host["W7"] = synthetic.mxfp8_linear()[1]
         self.d = {k: t(v) for k, v in self.host.items()}
         u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
         f32 = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)
@@ -192,6 +201,13 @@ class Workload:
             self.Y5 = bf(4096, 2048)
             self.launches_per_step += 3
             self._outs += [self.Y5]
+        if "blk" in groups:
+            self.A7q = (u8(4096, 7168), f32(56, 4096), u8(4096 * 7168 // 32))
+            self.B7q = (u8(2048, 7168), f32(16, 56), u8(2048 * 7168 // 32))
+            self.W7q = (u8(14336, 4096), u8(sb(14336, 4096)), u8(4096, 14336), u8(sb(4096, 14336)))
+            self.Y7 = bf(4096, 2048)
+            self.launches_per_step += 6
+            self._outs += [self.Y7]
         if "mx4" in groups:
             self.A6q = (u8(8192, 4096), u8(sb(8192, 8192)))
             self.B6q = (u8(8192, 4096), u8(sb(8192, 8192)))
@@ -239,6 +255,21 @@ class Workload:
             mark("dsgemm")
             mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
                                   out=self.Y5)
+        if "blk" in g:
+            mark("blkq")
+            mx.mx_quantize(d["A7"], block=128, block_rows=1, sfmt=mx.SCALE_FP32_POW2, layout=mx.ROWWISE,
+                           q_row=self.A7q[0], s_row=self.A7q[1])
+            mx.mx_quantize(d["B7"], block=128, block_rows=128, sfmt=mx.SCALE_FP32_POW2, layout=mx.ROWWISE,
+                           q_row=self.B7q[0], s_row=self.B7q[1])
+            mark("blkconv")
+            mx.mx_scales_from_fp32_blocks(self.A7q[1], 4096, 7168, 1, out=self.A7q[2])
+            mx.mx_scales_from_fp32_blocks(self.B7q[1], 2048, 7168, 128, out=self.B7q[2])
+            mark("blkgemm")
+            mx.mx_gemm(self.A7q[0], self.A7q[2], mx.E4M3, self.B7q[0], self.B7q[2], mx.E4M3, 4096, 2048, 7168,
+                       mx.OUT_BF16, out=self.Y7)
+            mark("w2dq")
+            mx.mx_quantize(d["W7"], block=32, block_rows=32, layout=mx.BOTH, q_row=self.W7q[0], s_row=self.W7q[1],
+                           q_col=self.W7q[2], s_col=self.W7q[3])
         if "mx4" in g:
             mark("mx4q")
             for src, dst in ((d["A6"], self.A6q), (d["B6"], self.B6q)):
@@ -249,7 +280,8 @@ class Workload:
         mark("end")
 
 
-ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "mx4q", "mx4gemm"]
+ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
+             "w2dq", "mx4q", "mx4gemm"]
 
 
 def row_report(name, ms, peaks):
@@ -257,12 +289,14 @@ def row_report(name, ms, peaks):
     s = ms / 1e3
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (4.5 / 2.25 nominal)
     fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
-    if name in ("q2", "linq", "nvq", "dsq", "mx4q"):
-        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES}[name]
+    if name in ("q2", "linq", "nvq", "dsq", "mx4q", "blkq", "blkconv", "w2dq"):
+        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES,
+             "blkq": DSQ_BYTES, "blkconv": BLKCONV_BYTES, "w2dq": W2DQ_BYTES}[name]
         gbs = b / s / 1e9
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
-    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4}[name]
+    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
+         "blkgemm": F_DS}[name]
     tf = f / s / 1e12
     peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
@@ -441,7 +475,7 @@ def main():
     ap.add_argument("--library-reference", action="store_true",
                     help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
-                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4 is measured only here) for profiling runs; "
+                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4 and blk are measured only here) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -520,18 +554,22 @@ def main():
     rows_ms = {n: v / args.steps for n, v in rows_ms.items()}
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
-    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4}
+    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
+                 "blkgemm": F_DS}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
     kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
                "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"],
-               "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"]}
+               "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
+               "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
+               "mx_quantize_2d32": ["w2dq"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
-                "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2}
+                "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
+                "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -540,9 +578,9 @@ def main():
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm"):
+    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks"):
         flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
-                 "mxfp4_gemm": F_MX4}[dom]
+                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS}[dom]
         fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm")
         peak = 3 * fp8_peak if fp4 else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12

@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) block-scaled quantization and GEMMs: MXFP8, NVFP4, DeepSeek FP8.
+"""GB300 (sm_103a) block-scaled quantization and GEMMs: MXFP8, MXFP4, NVFP4, DeepSeek FP8.
 
 Thin Python binding over the C ABI of ``libmxgb.so`` (declared in include/mx.h).
 Every function here only marshals arguments: tensors are torch CUDA tensors
@@ -8,7 +8,7 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
-  mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
+  mx_scales_from_fp32_blocks, mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
 
@@ -23,14 +23,14 @@ from .build import LIB as _LIB_PATH
 # enums (include/mx.h)
 MX_OK, MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED, MX_ERR_CUDA, MX_ERR_TIMEOUT = range(5)
 E4M3, E5M2, E2M1 = 0, 1, 2
-SCALE_E8M0, SCALE_UE4M3, SCALE_FP32 = 0, 1, 2
+SCALE_E8M0, SCALE_UE4M3, SCALE_FP32, SCALE_FP32_POW2 = 0, 1, 2, 3
 ROWWISE, COLWISE, BOTH = 1, 2, 3
 OUT_F32, OUT_BF16 = 0, 1
 
 EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
-    "nvfp4_quantize_noalloc", "mx_quantize_dual",
+    "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks",
 )
 
 
@@ -73,6 +73,7 @@ def load():
             "mx_num_sms": (i32, []),
             "nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
             "mx_quantize_dual": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "mx_scales_from_fp32_blocks": (i32, [vp, i64, i64, i32, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -139,7 +140,7 @@ def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int
     rows, cols = x.shape
     dev = x.device
     row, col = bool(layout & ROWWISE), bool(layout & COLWISE)
-    if sfmt == SCALE_FP32:
+    if sfmt in (SCALE_FP32, SCALE_FP32_POW2):
         if row and q_row is None:
             q_row = torch.empty(rows, cols, dtype=torch.uint8, device=dev)
         if row and s_row is None:
@@ -161,6 +162,18 @@ def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int
                             _ptr(q_col) if col else None, _ptr(s_col) if col else None, _stream(stream))
     _check(st, "mx_quantize")
     return (q_row if row else None, s_row if row else None, q_col if col else None, s_col if col else None)
+
+
+def mx_scales_from_fp32_blocks(s: torch.Tensor, rows: int, cols: int, block_rows: int, out=None, stream=None):
+    """Per-32 E8M0 scales (MX GEMM layout, flat uint8) for a [rows][cols] code matrix from its
+    power-of-two FP32 block scales (include/mx.h, mx_scales_from_fp32_blocks)."""
+    if s.dtype != torch.float32:
+        raise ValueError("s must be float32")
+    if out is None:
+        out = _u8(rows * cols // 32, s.device)
+    st = load().mx_scales_from_fp32_blocks(_ptr(s), rows, cols, block_rows, _ptr(out), _stream(stream))
+    _check(st, "mx_scales_from_fp32_blocks")
+    return out
 
 
 def mx_quantize_dual(x: torch.Tensor, layout: int = BOTH, e4m3=None, e5m2=None, stream=None):

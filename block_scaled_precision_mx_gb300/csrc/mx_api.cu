@@ -181,11 +181,22 @@ bool quant_grid(int64_t row_tiles, int64_t col_tiles, dim3* g) {
 }
 
 mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int f0, int nf, bool row, bool col,
-                             const MxOut& o, cudaStream_t st) {
+                             const MxOut& o, cudaStream_t st, bool b2d = false) {
   dim3 grid;
   if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
 #define MXQ(F, N, R, C) mx_quantize_kernel<F, N, R, C><<<grid, 256, 0, st>>>(x, rows, cols, o)
-  if (nf == 2) {
+#define MXQ2D(F, R, C) mx_quantize_kernel<F, 1, R, C, true><<<grid, 256, 0, st>>>(x, rows, cols, o)
+  if (b2d) {  // 2-D 32x32 blocks, MXFP8 only
+    if (f0 == 0) {
+      if (row && col) MXQ2D(0, true, true);
+      else if (row) MXQ2D(0, true, false);
+      else MXQ2D(0, false, true);
+    } else {
+      if (row && col) MXQ2D(1, true, true);
+      else if (row) MXQ2D(1, true, false);
+      else MXQ2D(1, false, true);
+    }
+  } else if (nf == 2) {
     if (row && col) MXQ(0, 2, true, true);
     else if (row) MXQ(0, 2, true, false);
     else MXQ(0, 2, false, true);
@@ -203,6 +214,7 @@ mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int 
     else MXQ(1, 1, false, true);
   }
 #undef MXQ
+#undef MXQ2D
   return launch_status();
 }
 
@@ -236,10 +248,12 @@ int mx_num_sms(void) { return g_last_sms; }
 
 size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_scale_fmt sfmt) {
   if (rows <= 0 || cols <= 0) return 0;
-  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0) return static_cast<size_t>(rows * (cols / 32));
+  if (block == 32 && (block_rows == 1 || block_rows == 32) && sfmt == MX_SCALE_E8M0)
+    return static_cast<size_t>(rows * (cols / 32));  // 32x32 blocks are stored expanded per 1x32
   if (block == 16 && block_rows == 1 && sfmt == MX_SCALE_UE4M3) return static_cast<size_t>(rows * (cols / 16));
-  if (block == 128 && block_rows == 1 && sfmt == MX_SCALE_FP32) return static_cast<size_t>(4 * rows * (cols / 128));
-  if (block == 128 && block_rows == 128 && sfmt == MX_SCALE_FP32)
+  const bool f32 = sfmt == MX_SCALE_FP32 || sfmt == MX_SCALE_FP32_POW2;
+  if (block == 128 && block_rows == 1 && f32) return static_cast<size_t>(4 * rows * (cols / 128));
+  if (block == 128 && block_rows == 128 && f32)
     return static_cast<size_t>(4 * (rows / 128) * (cols / 128));
   return 0;
 }
@@ -250,13 +264,16 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
   if (!x || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MX_ERR_INVALID_ARG;
   if (rows > (1ll << 31) || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
   if (elem != MX_E4M3 && elem != MX_E5M2 && elem != MX_E2M1) return MX_ERR_INVALID_ARG;
-  if (sfmt != MX_SCALE_E8M0 && sfmt != MX_SCALE_UE4M3 && sfmt != MX_SCALE_FP32) return MX_ERR_INVALID_ARG;
+  if (sfmt != MX_SCALE_E8M0 && sfmt != MX_SCALE_UE4M3 && sfmt != MX_SCALE_FP32 && sfmt != MX_SCALE_FP32_POW2)
+    return MX_ERR_INVALID_ARG;
   if (layout != MX_ROWWISE && layout != MX_COLWISE && layout != MX_BOTH) return MX_ERR_INVALID_ARG;
   if (!aligned(x, 16)) return MX_ERR_INVALID_ARG;
   cudaStream_t st = as_stream(stream);
   const bool row = (layout & MX_ROWWISE) != 0, col = (layout & MX_COLWISE) != 0;
 
-  if (block == 32 && block_rows == 1 && sfmt == MX_SCALE_E8M0) {  // MXFP8 (E4M3, E5M2) or MXFP4 (E2M1)
+  const bool b2d = block_rows == 32;  // 2-D 32x32 blocks (MXFP8 weights)
+  if (block == 32 && (block_rows == 1 || (b2d && elem != MX_E2M1)) && sfmt == MX_SCALE_E8M0) {
+    // MXFP8 (E4M3, E5M2) or MXFP4 (E2M1); 1x32 blocks, or 32x32 blocks for MXFP8
     if (row && (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 16))) return MX_ERR_INVALID_ARG;
     if (col && (!q_col || !s_col || !aligned(q_col, 16) || !aligned(s_col, 16))) return MX_ERR_INVALID_ARG;
     const int64_t tiles = (rows / 128) * (cols / 128);
@@ -267,24 +284,24 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     o.q_col[0] = static_cast<uint8_t*>(q_col);
     o.s_col[0] = static_cast<uint8_t*>(s_col);
     const int f0 = elem == MX_E4M3 ? 0 : (elem == MX_E5M2 ? 1 : 2);
-    return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, f0, 1, row, col, o, st);
+    return launch_mx_quantize(static_cast<const uint16_t*>(x), rows, cols, f0, 1, row, col, o, st, b2d);
   }
-  if (block == 128 && sfmt == MX_SCALE_FP32 && elem == MX_E4M3 && layout == MX_ROWWISE &&
-      (block_rows == 1 || block_rows == 128)) {
+  if (block == 128 && (sfmt == MX_SCALE_FP32 || sfmt == MX_SCALE_FP32_POW2) && elem == MX_E4M3 &&
+      layout == MX_ROWWISE && (block_rows == 1 || block_rows == 128)) {
     if (!q_row || !s_row || !aligned(q_row, 16) || !aligned(s_row, 4)) return MX_ERR_INVALID_ARG;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
+    auto* qo = static_cast<uint8_t*>(q_row);
+    auto* so = static_cast<float*>(s_row);
+    const bool pow2 = sfmt == MX_SCALE_FP32_POW2;
+    dim3 grid;
     if (block_rows == 1) {
-      dim3 grid;
       if (!quant_grid(rows / 64, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-      ds_quantize_1x128_kernel<<<grid, 256, 0, st>>>(xb, rows, cols,
-                                                                            static_cast<uint8_t*>(q_row),
-                                                                            static_cast<float*>(s_row));
+      if (pow2) ds_quantize_1x128_kernel<true><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
+      else ds_quantize_1x128_kernel<false><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
     } else {
-      dim3 grid;
       if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-      ds_quantize_128x128_kernel<<<grid, 256, 0, st>>>(xb, rows, cols,
-                                                                              static_cast<uint8_t*>(q_row),
-                                                                              static_cast<float*>(s_row));
+      if (pow2) ds_quantize_128x128_kernel<true><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
+      else ds_quantize_128x128_kernel<false><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
     }
     return launch_status();
   }
@@ -364,6 +381,18 @@ size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols) {
   (void)rows;
   (void)cols;
   return 16;
+}
+
+mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols, int block_rows, void* s_e8m0,
+                                     void* stream) {
+  if (!s || !s_e8m0 || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MX_ERR_INVALID_ARG;
+  if (block_rows != 1 && block_rows != 128) return MX_ERR_INVALID_ARG;
+  if (!aligned(s, 4) || !aligned(s_e8m0, 16)) return MX_ERR_INVALID_ARG;
+  dim3 grid;
+  if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
+  mx_scales_from_blocks_kernel<<<grid, 128, 0, as_stream(stream)>>>(s, rows, cols, block_rows,
+                                                                      static_cast<uint8_t*>(s_e8m0));
+  return launch_status();
 }
 
 mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* q_packed, void* s_ue4m3, float* gscale,

@@ -162,12 +162,17 @@ __device__ __forceinline__ uint32_t mx_cvt2(float lo, float hi) {
 
 // NF = 1: format F0 only; NF = 2: E4M3 and E5M2 from the same read of x (F0 = 0).
 // Four resident CTAs per SM (64 registers a thread) keep enough loads in flight.
-template <int F0, int NF, bool ROW, bool COL>
+// B2D: 2-D 32x32 blocks (one scale per 32x32 block of x, the MX rule over the whole block;
+// "MXFP8 on SM120: software support" (xuesongtap.github.io), sec 1.3).  Both copies then carry
+// the block's scale on each of their 1x32 blocks, so the transposed copy's codes are the
+// transpose of the row-wise codes.
+template <int F0, int NF, bool ROW, bool COL, bool B2D = false>
 __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, const MxOut o) {
   __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 1];  // 128 rows x 128 bf16 (as bf16x2 words)
   __shared__ __align__(16) uint8_t srow[NF][512];
   __shared__ __align__(16) uint8_t scol[NF][512];
+  __shared__ uint32_t bmax[B2D ? 16 : 1];  // 2-D: largest |x| bits of the tile's 4 x 4 blocks
 
   // grid: x = row tile, y = column tile (no 64-bit division per thread)
   const int64_t tiles_c = cols >> 7;
@@ -188,13 +193,35 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
       *reinterpret_cast<uint4*>(&tile[(r0 + 16 * i) * 64 + lc * 4]) = v[i];
   }
 
+  if constexpr (B2D) {
+    // block (br, bc): rows 32 br .. (this thread's rows r0 + 16 i with i >> 1 == br), columns
+    // 32 bc .. (lc >> 2 == bc); the 4 lanes of a block column and the two r0 of a warp combine
+    // by shuffles, the 8 warps through shared memory
+    if (t < 16) bmax[t] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int br = 0; br < 4; ++br) {
+      uint32_t m = max(absmax_bits8(v[2 * br]), absmax_bits8(v[2 * br + 1]));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+      if ((t & 19) == 0) atomicMax(&bmax[br * 4 + (lc >> 2)], m);  // lc % 4 == 0, even r0
+    }
+    __syncthreads();
+  }
+
   if (ROW) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = r0 + 16 * i;
-      uint32_t m = absmax_bits8(v[i]);
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-      m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      uint32_t m;
+      if constexpr (B2D) {
+        m = bmax[(i >> 1) * 4 + (lc >> 2)];
+      } else {
+        m = absmax_bits8(v[i]);
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+      }
       if constexpr (F0 == 2) {  // MXFP4: packed E2M1, a NaN or Inf block gets codes 0x7
         uint32_t packed, sbyte;
         if (m >= 0x7F80u) {
@@ -249,6 +276,10 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) m[j] = max(m[j], __shfl_xor_sync(0xFFFFFFFFu, m[j], 1));
+    if constexpr (B2D) {  // the 32x32 block's maximum instead of the column block's
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m[j] = bmax[rb * 4 + ((4 * cq + j) >> 5)];
+    }
     if constexpr (F0 == 2) {  // MXFP4: 16 codes per column -> 8 bytes
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -334,11 +365,59 @@ __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __r
 }
 
 // ---------------------------------------------------------------------------------------------
+// Power-of-two block scales and their E8M0 form
+// ---------------------------------------------------------------------------------------------
+// 2^n as an FP32 for -127 <= n <= 127 (2^-127 is the subnormal 0x00400000)
+__device__ __forceinline__ float pow2f(int n) {
+  return __uint_as_float(n >= -126 ? static_cast<uint32_t>(n + 127) << 23 : 0x00400000u);
+}
+
+// k = the smallest integer with 448 * 2^k >= amax, clamped to [-127, 127], from the bf16 bits of
+// amax (finite, sign cleared); 0 when amax == 0.  448 = 1.75 * 2^8 and 1.75 is the bf16
+// mantissa 0x60: amax = 1.m * 2^e needs k = e - 8 when 1.m <= 1.75 and e - 7 otherwise.  A bf16
+// subnormal amax is below 448 * 2^-127 and gets the clamp.
+__device__ __forceinline__ int pow2_scale_exp(uint32_t amax_bits) {
+  if (amax_bits == 0) return 0;
+  const int e = static_cast<int>(amax_bits >> 7);
+  if (e == 0) return -127;
+  const int k = (e - 127) - 8 + ((amax_bits & 0x7Fu) > 0x60u ? 1 : 0);
+  return k < -127 ? -127 : (k > 127 ? 127 : k);
+}
+
+// E8M0 code of an FP32 scale: k + 127 for exactly 2^k, -127 <= k <= 127; otherwise 0xFF (NaN)
+__device__ __forceinline__ uint32_t e8m0_of_pow2(float sc) {
+  const uint32_t b = __float_as_uint(sc);
+  if (b == 0x00400000u) return 0;                           // 2^-127
+  const uint32_t e = b >> 23;                               // sign bit set -> e > 255
+  return ((b & 0x7FFFFFu) == 0 && e >= 1 && e <= 254) ? e : 0xFFu;
+}
+
+// Per-32 E8M0 scales in the MX GEMM layout of a [rows][cols] code matrix from power-of-two FP32
+// block scales: block_rows 1 -> s float[cols/128][rows] (1x128 tiles), block_rows 128 -> s
+// float[rows/128][cols/128].  The four 32-blocks of a 128-block keep its scale; a 2-D block's
+// scale is broadcast to its 128 rows.  Grid: x = 128-row block, y = 128-column chunk; one thread
+// per row writes the row's 4 bytes of the chunk.
+__global__ void __launch_bounds__(128) mx_scales_from_blocks_kernel(const float* __restrict__ s, int64_t rows,
+                                                                    int64_t cols, int block_rows,
+                                                                    uint8_t* __restrict__ out) {
+  const int64_t rb = blockIdx.x, kc = blockIdx.y;
+  const int i = threadIdx.x;
+  const int64_t nkc = cols >> 7;
+  const float sc = (block_rows == 1) ? s[kc * rows + rb * 128 + i] : s[rb * nkc + kc];
+  const uint32_t code = e8m0_of_pow2(sc);
+  *reinterpret_cast<uint32_t*>(out + (rb * nkc + kc) * 512 + chunk_offset(i, 0)) = code * 0x01010101u;
+}
+
+// ---------------------------------------------------------------------------------------------
 // DeepSeek 1x128: s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored
 // [K/128][rows].  CTA = 64 rows x one 128-column k-block; 4 lanes per row, 32 bf16 per lane (four
 // 128-bit loads, the row's 4 lanes covering 64 contiguous bytes per load), so the per-row scale
 // and reciprocal are computed by 4 lanes, not 16.
 // ---------------------------------------------------------------------------------------------
+// POW2: Float8BlockScaling with power-of-two scales ("MXFP8 on SM120: software support"
+// (xuesongtap.github.io), sec 1.3): s = 2^k, k the smallest integer with 448 * 2^k >= amax
+// (clamped to [-127, 127]; 0 when amax == 0), q = E4M3(x * 2^-k), which is exact scaling.
+template <bool POW2>
 __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ q,
                                                                 float* __restrict__ s) {
@@ -353,7 +432,14 @@ __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* 
   uint32_t m = max(max(absmax_bits8(v[0]), absmax_bits8(v[1])), max(absmax_bits8(v[2]), absmax_bits8(v[3])));
   m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
   m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-  const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  float sc, inv = 1.0f;
+  if (POW2) {
+    const int k = pow2_scale_exp(m);
+    sc = pow2f(k);
+    inv = pow2f(-k);
+  } else {
+    sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  }
   const bool fast = QuotientBracket::usable(sc);
   const QuotientBracket qb(fast ? sc : 1.0f);
   uint8_t* qr = q + r * cols + kb * 128;
@@ -364,7 +450,8 @@ __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float a = bf16_bits_to_float(w[j] & 0xFFFFu), b = bf16_bits_to_float(w[j] >> 16);
-      p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
+      if (POW2) p[j] = cvt_e4m3x2(__fmul_rn(a, inv), __fmul_rn(b, inv));
+      else p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
     }
     *reinterpret_cast<uint2*>(qr + (4 * i + l4) * 8) = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
   }
@@ -372,6 +459,7 @@ __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* 
 }
 
 // DeepSeek 128x128 weight blocks: one CTA per block; 256 threads x 64 elements in registers.
+template <bool POW2>
 __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                   int64_t cols, uint8_t* __restrict__ q,
                                                                   float* __restrict__ s) {
@@ -395,7 +483,14 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
   m = wmax[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
-  const float sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  float sc, inv = 1.0f;
+  if (POW2) {
+    const int k = pow2_scale_exp(m);
+    sc = pow2f(k);
+    inv = pow2f(-k);
+  } else {
+    sc = (m == 0) ? 1.0f : __fdiv_rn(bf16_bits_to_float(m), 448.0f);
+  }
   const bool fast = QuotientBracket::usable(sc);
   const QuotientBracket qb(fast ? sc : 1.0f);
 #pragma unroll
@@ -405,7 +500,8 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float a = bf16_bits_to_float(w[j] & 0xFFFFu), b = bf16_bits_to_float(w[j] >> 16);
-      p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
+      if (POW2) p[j] = cvt_e4m3x2(__fmul_rn(a, inv), __fmul_rn(b, inv));
+      else p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
     }
     *reinterpret_cast<uint2*>(q + (br * 128 + r0 + 16 * i) * cols + bc * 128 + lc * 8) =
         make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));

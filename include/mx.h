@@ -64,7 +64,7 @@ typedef enum {
 } mx_status;
 
 typedef enum { MX_E4M3 = 0, MX_E5M2 = 1, MX_E2M1 = 2 } mx_elem;
-typedef enum { MX_SCALE_E8M0 = 0, MX_SCALE_UE4M3 = 1, MX_SCALE_FP32 = 2 } mx_scale_fmt;
+typedef enum { MX_SCALE_E8M0 = 0, MX_SCALE_UE4M3 = 1, MX_SCALE_FP32 = 2, MX_SCALE_FP32_POW2 = 3 } mx_scale_fmt;
 typedef enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_BOTH = 3 } mx_layout;
 typedef enum { MX_OUT_F32 = 0, MX_OUT_BF16 = 1 } mx_out;
 
@@ -93,11 +93,20 @@ const char* mx_status_string(mx_status s);
  *       matrix.  Pointers of a copy that is not requested may be NULL.
  *       MXFP4 codes are packed two per byte, element 2i in the low nibble:
  *       q_row[rows][cols/2], q_col[cols][rows/2].
+ *  1b. MX with 2-D weight blocks: block = 32, block_rows = 32, elem = MX_E4M3 or MX_E5M2,
+ *     sfmt = MX_SCALE_E8M0 ([MX] sec 1.3): one scale per 32x32 block of x by the rule of 1
+ *     over the whole block, stored expanded exactly as in 1 (every 1x32 block of a row-wise
+ *     row and of a column-wise row carries its 32x32 block's scale), so mx_gemm consumes it
+ *     unchanged; the column-wise codes are the transpose of the row-wise ones.
  *  2. DeepSeek activations: block = 128, block_rows = 1, elem = MX_E4M3,
  *     sfmt = MX_SCALE_FP32, layout = ROWWISE; rows % 128 == 0, cols % 128 == 0.
  *     s = fl32(amax / 448) (1.0 when amax == 0); q = RNE-satfinite(fl32(x / s)).
  *       q_row[rows][cols] u8, s_row float[cols/128][rows].
  *  3. DeepSeek weights: block = 128, block_rows = 128, otherwise as 2.
+ *  2/3 with sfmt = MX_SCALE_FP32_POW2: Float8BlockScaling with power-of-two scales ([MX]
+ *     sec 1.3): s = 2^k with k the smallest integer such that 448 * 2^k >= amax (clamped to
+ *     [-127, 127]; s = 1 when amax == 0), q = RNE-satfinite(x * 2^-k); same layouts as 2/3.
+ *     mx_scales_from_fp32_blocks turns these scales into MX scales for mx_gemm.
  *       q_row[rows][cols] u8, s_row float[rows/128][cols/128].
  *     Inputs for 2 and 3 must be finite.
  */
@@ -133,6 +142,21 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea,
                   const void* qb, const void* sb, mx_elem eb,
                   int64_t M, int64_t N, int64_t K,
                   void* out, mx_out out_dtype, int64_t ldc, void* stream);
+
+/*
+ * mx_scales_from_fp32_blocks -- Float8BlockScaling scales in MX form.  [MX] sec 1.3.
+ *
+ * s: power-of-two FP32 block scales as mx_quantize(block = 128, sfmt = MX_SCALE_FP32_POW2)
+ * writes them: block_rows = 1 -> float[cols/128][rows] (1x128 tiles of a [rows][cols] code
+ * matrix), block_rows = 128 -> float[rows/128][cols/128] (128x128 blocks); 4-byte aligned.
+ * s_e8m0: rows*cols/32 bytes (16-byte aligned), written in the MX GEMM layout of the
+ * [rows][cols] code matrix: each 1x32 block gets its 128-block's scale 2^k as the E8M0 code
+ * k + 127; a scale that is not exactly 2^k with -127 <= k <= 127 becomes the E8M0 NaN code 0xFF
+ * (products that use it are NaN).  The E4M3 codes are passed to mx_gemm as they are.
+ * rows % 128 == 0, cols % 128 == 0, block_rows 1 or 128, else MX_ERR_INVALID_ARG.
+ */
+mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols, int block_rows, void* s_e8m0,
+                                     void* stream);
 
 /* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
@@ -197,9 +221,10 @@ mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols,
                                  void* q_packed, void* s_ue4m3, float* gscale, void* stream);
 
 /* Bytes of the scale tensor mx_quantize / nvfp4_quantize write for a [rows][cols] input:
- * block 32 + E8M0 -> rows*cols/32; block 16 + UE4M3 -> rows*cols/16; block 128 + FP32 ->
- * 4*rows*cols/128 (block_rows 1) or 4*(rows/128)*(cols/128) (block_rows 128).  0 if the
- * combination is not supported. */
+ * block 32 + E8M0 -> rows*cols/32 (block_rows 1, and 32: 2-D blocks are stored expanded);
+ * block 16 + UE4M3 -> rows*cols/16; block 128 + FP32 or FP32_POW2 -> 4*rows*cols/128
+ * (block_rows 1) or 4*(rows/128)*(cols/128) (block_rows 128).  0 if the combination is not
+ * supported. */
 size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_scale_fmt sfmt);
 
 /*

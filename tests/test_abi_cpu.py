@@ -76,6 +76,21 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(block=128, sfmt=2, layout=2) == mx.MX_ERR_UNSUPPORTED   # DeepSeek column-wise
     assert call(elem=2, block=16) == mx.MX_ERR_UNSUPPORTED  # E2M1 blocks of 16 with E8M0: not MX
     assert call(rows=128, cols=65536 * 128) == mx.MX_ERR_INVALID_ARG   # more than 65535 column tiles
+    assert call(block_rows=32, elem=2) == mx.MX_ERR_UNSUPPORTED      # 2-D blocks are MXFP8 only
+    assert call(sfmt=3) == mx.MX_ERR_UNSUPPORTED                     # power-of-two FP32 needs block 128
+    assert call(block=128, sfmt=3, layout=3) == mx.MX_ERR_UNSUPPORTED
+    assert call(sfmt=4) == mx.MX_ERR_INVALID_ARG
+
+
+def test_scale_conversion_rejects_bad_arguments(lib):
+    c = lib.mx_scales_from_fp32_blocks
+    assert c(None, 128, 128, 1, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert c(FAKE, 100, 128, 1, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert c(FAKE, 128, 128, 32, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert c(FAKE, 128, 128, 1, FAKE + 8, None) == mx.MX_ERR_INVALID_ARG
+    assert c(FAKE + 2, 128, 128, 128, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert mx.mx_scale_bytes(256, 512, 32, 32, mx.SCALE_E8M0) == 256 * 16
+    assert mx.mx_scale_bytes(256, 512, 128, 128, mx.SCALE_FP32_POW2) == 4 * 2 * 4
 
 
 def test_dual_quantize_rejects_bad_arguments(lib):
