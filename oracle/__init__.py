@@ -76,6 +76,10 @@ def _load():
                 "orc_e8m0_of_scale": (ctypes.c_uint8, [f32]),
                 "orc_mx_scales_from_blocks": (None, [p, i64, i64, i32, p]),
                 "orc_mx_quantize_2d32": (None, [p, i64, i64, i32, p, p]),
+                "orc_fwht16_f32": (None, [p, u32]),
+                "orc_e2m1_stochastic": (ctypes.c_uint8, [f32, ctypes.c_uint8]),
+                "orc_nv_quantize_ex": (None, [p, i64, i64, i32, u32, p, p, p, ctypes.POINTER(f32)]),
+                "orc_nv_quantize_2d16": (None, [p, i64, i64, p, p, ctypes.POINTER(f32)]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -247,6 +251,43 @@ def nv_quantize(x):
     s = np.empty((rows, cols // 16), np.uint8)
     sg = ctypes.c_float(0.0)
     _load().orc_nv_quantize(_ptr(xb), rows, cols, _ptr(q), _ptr(s), ctypes.byref(sg))
+    return q, s, sg.value
+
+
+# ---------------------------------------------------------------- NVFP4 training options
+def fwht16(v, signs: int = 0):
+    """FP32 16-point transform 0.25 * H16 * (d .* v) in the fixed butterfly order."""
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32).copy())
+    _load().orc_fwht16_f32(_ptr(a), signs)
+    return a
+
+
+def e2m1_stochastic(y: float, r: int) -> int:
+    return _load().orc_e2m1_stochastic(y, r)
+
+
+def nv_quantize_ex(x, rht: bool = False, signs: int = 0, rbits=None):
+    """NVFP4 with the transform and/or stochastic rounding: (codes [rows][cols] unpacked,
+    s [rows][cols/16], s_global)."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 16), np.uint8)
+    sg = ctypes.c_float(0.0)
+    rb = None if rbits is None else np.ascontiguousarray(rbits, dtype=np.uint8)
+    _load().orc_nv_quantize_ex(_ptr(xb), rows, cols, int(bool(rht)), signs, None if rb is None else _ptr(rb),
+                               _ptr(q), _ptr(s), ctypes.byref(sg))
+    return q, s, sg.value
+
+
+def nv_quantize_2d16(x):
+    """NVFP4 with 16x16 blocks: (codes [rows][cols] unpacked, s [rows/16][cols/16], s_global)."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows // 16, cols // 16), np.uint8)
+    sg = ctypes.c_float(0.0)
+    _load().orc_nv_quantize_2d16(_ptr(xb), rows, cols, _ptr(q), _ptr(s), ctypes.byref(sg))
     return q, s, sg.value
 
 

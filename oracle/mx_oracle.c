@@ -497,6 +497,122 @@ void orc_nv_quantize(const uint16_t* x, int64_t rows, int64_t cols,
 }
 
 /* ---------------------------------------------------------------------- */
+/* NVFP4 training options, [DS] sec 13 ("from FP8 to 4 bits": a 16x16     */
+/* random Hadamard transform, stochastic rounding, 16x16 2-D weight       */
+/* blocks) and [NV] sec 3.2 (stochastic rounding: round up or down with   */
+/* probability set by the distance, E[Q(x) - x] = 0).                      */
+/* Readings (the pages give no formulas beyond these):                     */
+/*  - the transform acts on every 1x16 block along the reduction axis:     */
+/*    v = 0.25 * H16 * (d .* x), d_i = -1 where bit i of a 16-bit sign     */
+/*    mask is set, H16 the Sylvester Hadamard matrix; in FP32 with the    */
+/*    butterfly order h = 1, 2, 4, 8 below (both sides use this order);    */
+/*    the NVFP4 recipe then runs on v (global amax included);              */
+/*  - stochastic rounding takes one random byte r per element (an input):  */
+/*    for a = |fl32(v / s_hat)| below 6 with E2M1 neighbours lo <= a < hi, */
+/*    round up iff r < floor(256 * (a - lo) / (hi - lo)); a >= 6 gives 6;  */
+/*    so E[Q] - a lies in (-(hi - lo)/256, 0] and is 0 when 256 (a - lo)  */
+/*    / (hi - lo) is an integer;                                           */
+/*  - 2-D blocks: the block maximum runs over 16x16 elements; W and W^T    */
+/*    then hold the same codes and scales.                                 */
+/* ---------------------------------------------------------------------- */
+void orc_fwht16_f32(float v[16], uint32_t signs) {
+    for (int i = 0; i < 16; ++i)
+        if ((signs >> i) & 1u) v[i] = -v[i];
+    for (int h = 1; h < 16; h <<= 1)
+        for (int i = 0; i < 16; ++i)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+    for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
+}
+
+/* E2M1 code of a by stochastic rounding with random byte r (sign from y) */
+uint8_t orc_e2m1_stochastic(float y, uint8_t r) {
+    static const double grid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t sign = signbit(y) ? 0x8 : 0x0;
+    double a = fabs((double)y);
+    int lo = 0;
+    if (a >= 6.0) return (uint8_t)(sign | 7);
+    while (lo < 6 && grid[lo + 1] <= a) ++lo;        /* grid[lo] <= a < grid[lo + 1] */
+    double frac = (a - grid[lo]) / (grid[lo + 1] - grid[lo]);
+    int up = (double)r < floor(256.0 * frac);
+    return (uint8_t)(sign | (lo + up));
+}
+
+/* NVFP4 quantization with the options above on x[rows][cols]:
+   rht != 0 applies the transform to every 1x16 block first; rbits != NULL
+   switches the element codes to stochastic rounding (rbits[rows][cols]).
+   Codes unpacked q[rows][cols] (4-bit values), block scales s[rows][cols/16]
+   (E4M3 codes), the global scale in *sg_out. */
+void orc_nv_quantize_ex(const uint16_t* x, int64_t rows, int64_t cols, int rht, uint32_t signs,
+                        const uint8_t* rbits, uint8_t* q, uint8_t* s, float* sg_out) {
+    int64_t nb = cols / 16;
+    float* v = (float*)malloc(sizeof(float) * (size_t)(rows * cols));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            float blk[16];
+            for (int i = 0; i < 16; ++i) blk[i] = bf16f(x[r * cols + b * 16 + i]);
+            if (rht) orc_fwht16_f32(blk, signs);
+            for (int i = 0; i < 16; ++i) v[r * cols + b * 16 + i] = blk[i];
+        }
+    float amax = 0.0f;
+    for (int64_t i = 0; i < rows * cols; ++i)
+        if (fabsf(v[i]) > amax) amax = fabsf(v[i]);
+    float sg = orc_nv_global_scale(amax);
+    *sg_out = sg;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* vb = v + r * cols + b * 16;
+            float bamax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                if (fabsf(vb[i]) > bamax) bamax = fabsf(vb[i]);
+            float sh;
+            s[r * nb + b] = orc_nv_block_scale(sg, bamax, &sh);
+            for (int i = 0; i < 16; ++i) {
+                int64_t o = r * cols + b * 16 + i;
+                if (!rbits) {
+                    q[o] = orc_nv_encode(vb[i], sh);
+                } else if (sh == 0.0f) {
+                    q[o] = 0;
+                } else {
+                    volatile float y = vb[i] / sh;
+                    q[o] = orc_e2m1_stochastic(y, rbits[o]);
+                }
+            }
+        }
+    free(v);
+}
+
+/* NVFP4 with 16x16 2-D blocks: codes q[rows][cols] (unpacked), block scales
+   s[rows/16][cols/16] (E4M3 codes), global scale *sg_out */
+void orc_nv_quantize_2d16(const uint16_t* x, int64_t rows, int64_t cols,
+                          uint8_t* q, uint8_t* s, float* sg_out) {
+    float sg = orc_nv_global_scale(orc_nv_amax(x, rows * cols));
+    *sg_out = sg;
+    int64_t nbr = rows / 16, nbc = cols / 16;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t br = 0; br < nbr; ++br)
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            float bamax = 0.0f;
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    float a = fabsf(bf16f(x[(br * 16 + i) * cols + bc * 16 + j]));
+                    if (a > bamax) bamax = a;
+                }
+            float sh;
+            s[br * nbc + bc] = orc_nv_block_scale(sg, bamax, &sh);
+            for (int i = 0; i < 16; ++i)
+                for (int j = 0; j < 16; ++j) {
+                    int64_t o = (br * 16 + i) * cols + bc * 16 + j;
+                    q[o] = orc_nv_encode(bf16f(x[o]), sh);
+                }
+        }
+}
+
+/* ---------------------------------------------------------------------- */
 /* Reference products in double.                                          */
 /* C[m][n] = sum_k A[m][k] B[n][k]; both operands K-contiguous.            */
 /* Each returns out[i][n] and absum[i][n] = sum_k |a_k b_k| for the rows   */
