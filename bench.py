@@ -12,6 +12,9 @@ One step = one pass over every row of the hot path, each on its own seeded synth
 An extra group, not part of the default step, is measured with --only mx4:
   mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
        with the block scales in the MMA (FP32 out)
+  nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
+       stochastic rounding (random bytes read from HBM), both, and 16x16 2-D blocks written in
+       both orientations
   blk  Float8BlockScaling through the MX GEMM at the DeepSeek shape (M=4096 K=7168 N=2048):
        power-of-two 1x128 / 128x128 quantize, scale conversion to E8M0, MXFP8 GEMM (bf16 out);
        and 2-D 32x32 MX quantize of the 14336x4096 weight (row- and column-wise)
@@ -72,6 +75,9 @@ MX4Q_BYTES = 2 * 8192 * 8192 * (2 + 0.5 + 1 / 32)
 # scale conversion: read the FP32 block scales, write one E8M0 byte per 32 elements
 BLKCONV_BYTES = 4 * 4096 * 56 + 4 * 16 * 56 + (4096 + 2048) * 7168 // 32
 W2DQ_BYTES = mx_q_bytes(14336, 4096)
+NVT_RHT_BYTES = nv_q_bytes(8192, 8192)
+NVT_SR_BYTES = nv_q_bytes(8192, 8192) + 8192 * 8192          # + one random byte per element
+NVT_2D_BYTES = 8192 * 8192 * (2 + 2 + 2 * (0.5 + 1 / 16))       # both orientations
 
 
 def load_peaks():
@@ -168,6 +174,8 @@ class Workload:
             self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
         if "mx4" in groups:
             self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
+        if "nvt" in groups:
+            self.host["A8"] = synthetic.nvfp4_pair()[0]
         if "blk" in groups:
             self.host["A7"], self.host["B7"] = synthetic.deepseek_pair()
             self.host["W7"] = synthetic.mxfp8_linear()[1]
@@ -201,6 +209,14 @@ class Workload:
             self.Y5 = bf(4096, 2048)
             self.launches_per_step += 3
             self._outs += [self.Y5]
+        if "nvt" in groups:
+            g8 = torch.Generator(device="cpu").manual_seed(8100)
+            self.R8 = torch.randint(0, 256, (8192, 8192), dtype=torch.uint8, generator=g8).to(dev)
+            nsb = sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)
+            self.A8q = (u8(8192, 4096), u8(nsb), f32(1), u8(16))
+            self.A8t = (u8(8192, 4096), u8(nsb), u8(4096, 8192), u8(nsb))
+            self.launches_per_step += 8
+            self._outs += [self.A8q[0], self.A8t[0], self.A8t[2]]
         if "blk" in groups:
             self.A7q = (u8(4096, 7168), f32(56, 4096), u8(4096 * 7168 // 32))
             self.B7q = (u8(2048, 7168), f32(16, 56), u8(2048 * 7168 // 32))
@@ -255,6 +271,18 @@ class Workload:
             mark("dsgemm")
             mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
                                   out=self.Y5)
+        if "nvt" in g:
+            q = self.A8q
+            mark("nvq_rht")
+            mx.nvfp4_quantize_ex(d["A8"], rht=True, signs=0xB4D2, q_packed=q[0], s_ue4m3=q[1], gscale=q[2],
+                                 workspace=q[3])
+            mark("nvq_sr")
+            mx.nvfp4_quantize_ex(d["A8"], rbits=self.R8, q_packed=q[0], s_ue4m3=q[1], gscale=q[2], workspace=q[3])
+            mark("nvq_rht_sr")
+            mx.nvfp4_quantize_ex(d["A8"], rht=True, signs=0xB4D2, rbits=self.R8, q_packed=q[0], s_ue4m3=q[1],
+                                 gscale=q[2], workspace=q[3])
+            mark("nvq_2d")
+            mx.nvfp4_quantize_2d(d["A8"], out=self.A8t, gscale=q[2], workspace=q[3])
         if "blk" in g:
             mark("blkq")
             mx.mx_quantize(d["A7"], block=128, block_rows=1, sfmt=mx.SCALE_FP32_POW2, layout=mx.ROWWISE,
@@ -281,7 +309,7 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d"]
 
 
 def row_report(name, ms, peaks):
@@ -289,9 +317,11 @@ def row_report(name, ms, peaks):
     s = ms / 1e3
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (4.5 / 2.25 nominal)
     fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
-    if name in ("q2", "linq", "nvq", "dsq", "mx4q", "blkq", "blkconv", "w2dq"):
-        b = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES,
-             "blkq": DSQ_BYTES, "blkconv": BLKCONV_BYTES, "w2dq": W2DQ_BYTES}[name]
+    hbm_rows = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES,
+                "blkq": DSQ_BYTES, "blkconv": BLKCONV_BYTES, "w2dq": W2DQ_BYTES, "nvq_rht": NVT_RHT_BYTES,
+                "nvq_sr": NVT_SR_BYTES, "nvq_rht_sr": NVT_SR_BYTES, "nvq_2d": NVT_2D_BYTES}
+    if name in hbm_rows:
+        b = hbm_rows[name]
         gbs = b / s / 1e9
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
@@ -475,7 +505,7 @@ def main():
     ap.add_argument("--library-reference", action="store_true",
                     help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
-                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4 and blk are measured only here) for profiling runs; "
+                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4, blk and nvt are measured only here) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -563,13 +593,15 @@ def main():
                "mx_quantize": ["q2", "linq"], "nvfp4_quantize": ["nvq"], "ds_quantize": ["dsq"],
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
-               "mx_quantize_2d32": ["w2dq"]}
+               "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
+               "nvfp4_quantize_2d": ["nvq_2d"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
-                "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1}
+                "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None

@@ -8,7 +8,8 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
-  mx_scales_from_fp32_blocks, mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
+  mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
+  nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
 
@@ -30,7 +31,8 @@ OUT_F32, OUT_BF16 = 0, 1
 EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
-    "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks",
+    "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
+    "nvfp4_quantize_2d",
 )
 
 
@@ -74,6 +76,8 @@ def load():
             "nvfp4_quantize_noalloc": (i32, [vp, i64, i64, vp, vp, vp, vp]),
             "mx_quantize_dual": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "mx_scales_from_fp32_blocks": (i32, [vp, i64, i64, i32, vp, vp]),
+            "nvfp4_quantize_ex": (i32, [vp, i64, i64, i32, ctypes.c_uint32, vp, vp, vp, vp, vp, vp]),
+            "nvfp4_quantize_2d": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -218,6 +222,52 @@ def nvfp4_quantize(x: torch.Tensor, q_packed=None, s_ue4m3=None, gscale=None, wo
                                _ptr(workspace), _stream(stream))
     _check(st, "nvfp4_quantize")
     return q_packed, s_ue4m3, gscale
+
+
+def nvfp4_quantize_ex(x: torch.Tensor, rht: bool = False, signs: int = 0, rbits=None, q_packed=None,
+                      s_ue4m3=None, gscale=None, workspace=None, stream=None):
+    """NVFP4 with the 16-point random Hadamard transform (rht, 16-bit sign mask) and/or stochastic
+    rounding (rbits: uint8 [rows][cols] random bytes) (include/mx.h, nvfp4_quantize_ex).
+    Returns (q_packed, s_ue4m3, gscale) as nvfp4_quantize."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    if q_packed is None:
+        q_packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+    if s_ue4m3 is None:
+        s_ue4m3 = _u8(mx_scale_bytes(rows, cols, 16, 1, SCALE_UE4M3), dev)
+    if gscale is None:
+        gscale = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _u8(max(16, nvfp4_workspace_bytes(rows, cols)), dev)
+    st = load().nvfp4_quantize_ex(_ptr(x), rows, cols, int(bool(rht)), int(signs),
+                                  None if rbits is None else _ptr(rbits), _ptr(q_packed), _ptr(s_ue4m3),
+                                  _ptr(gscale), _ptr(workspace), _stream(stream))
+    _check(st, "nvfp4_quantize_ex")
+    return q_packed, s_ue4m3, gscale
+
+
+def nvfp4_quantize_2d(x: torch.Tensor, out=None, gscale=None, workspace=None, stream=None):
+    """NVFP4 with 16x16 blocks, both orientations (include/mx.h, nvfp4_quantize_2d).
+    Returns (q_row, s_row, q_col, s_col, gscale)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    rows, cols = x.shape
+    dev = x.device
+    if out is None:
+        out = (torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev),
+               _u8(mx_scale_bytes(rows, cols, 16, 1, SCALE_UE4M3), dev),
+               torch.empty(cols, rows // 2, dtype=torch.uint8, device=dev),
+               _u8(mx_scale_bytes(cols, rows, 16, 1, SCALE_UE4M3), dev))
+    if gscale is None:
+        gscale = torch.empty(1, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _u8(max(16, nvfp4_workspace_bytes(rows, cols)), dev)
+    st = load().nvfp4_quantize_2d(_ptr(x), rows, cols, *[_ptr(t) for t in out], _ptr(gscale), _ptr(workspace),
+                                  _stream(stream))
+    _check(st, "nvfp4_quantize_2d")
+    return (*out, gscale)
 
 
 # ------------------------------------------------------------------ GEMMs

@@ -395,29 +395,77 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
   return launch_status();
 }
 
-mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* q_packed, void* s_ue4m3, float* gscale,
-                         void* workspace, void* stream) {
-  if (!x || !q_packed || !s_ue4m3 || !gscale || !workspace) return MX_ERR_INVALID_ARG;
-  if (rows <= 0 || cols <= 0 || rows % 128 || cols % 64) return MX_ERR_INVALID_ARG;
-  if (rows > (1ll << 31) || cols > (1ll << 31)) return MX_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(q_packed, 16) || !aligned(s_ue4m3, 16) || !aligned(gscale, 4) ||
-      !aligned(workspace, 16))
-    return MX_ERR_INVALID_ARG;
-  cudaStream_t st = as_stream(stream);
-  auto* amax = static_cast<unsigned int*>(workspace);
+}  // extern "C"
+
+namespace {
+// Pass 1 of every NVFP4 quantizer: clear the workspace word, then the global maximum (of the
+// transformed values when rht).
+mx_status nvfp4_pass1(const uint16_t* x, int64_t rows, int64_t cols, unsigned int* amax, bool rht, uint32_t signs,
+                      cudaStream_t st) {
   if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), st) != cudaSuccess) return MX_ERR_CUDA;
   const int sms = device_sms();
   if (sms <= 0) return MX_ERR_CUDA;
   const int64_t nvec = rows * cols / 8;
   int64_t grid1 = (nvec + 255) / 256;
   if (grid1 > 8ll * sms) grid1 = 8ll * sms;
-  nvfp4_amax_kernel<<<static_cast<unsigned>(grid1), 256, 0, st>>>(static_cast<const uint16_t*>(x), nvec, amax);
-  if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
+  if (rht) nvfp4_amax_kernel<true><<<static_cast<unsigned>(grid1), 256, 0, st>>>(x, nvec, amax, signs);
+  else nvfp4_amax_kernel<false><<<static_cast<unsigned>(grid1), 256, 0, st>>>(x, nvec, amax);
+  return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
+}
+
+bool nvfp4_args_ok(const void* x, int64_t rows, int64_t cols, int64_t colmult, const void* q, const void* s,
+                   const float* gscale, const void* workspace) {
+  if (!x || !q || !s || !gscale || !workspace) return false;
+  if (rows <= 0 || cols <= 0 || rows % 128 || cols % colmult) return false;
+  if (rows > (1ll << 31) || cols > (1ll << 31)) return false;
+  return aligned(x, 16) && aligned(q, 16) && aligned(s, 16) && aligned(gscale, 4) && aligned(workspace, 16);
+}
+}  // namespace
+
+extern "C" {
+
+mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* q_packed, void* s_ue4m3, float* gscale,
+                         void* workspace, void* stream) {
+  return nvfp4_quantize_ex(x, rows, cols, 0, 0u, nullptr, q_packed, s_ue4m3, gscale, workspace, stream);
+}
+
+mx_status nvfp4_quantize_ex(const void* x, int64_t rows, int64_t cols, int use_rht, uint32_t rht_signs,
+                            const void* rbits, void* q_packed, void* s_ue4m3, float* gscale, void* workspace,
+                            void* stream) {
+  if (!nvfp4_args_ok(x, rows, cols, 64, q_packed, s_ue4m3, gscale, workspace)) return MX_ERR_INVALID_ARG;
+  if ((use_rht != 0 && use_rht != 1) || rht_signs > 0xFFFFu) return MX_ERR_INVALID_ARG;
+  if (rbits && !aligned(rbits, 16)) return MX_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  auto* amax = static_cast<unsigned int*>(workspace);
+  const auto* xb = static_cast<const uint16_t*>(x);
+  const mx_status p1 = nvfp4_pass1(xb, rows, cols, amax, use_rht != 0, rht_signs, st);
+  if (p1 != MX_OK) return p1;
   dim3 grid;
   if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), rows, cols,
-                                                                      static_cast<uint8_t*>(q_packed),
-                                                                      static_cast<uint8_t*>(s_ue4m3), gscale, amax);
+  auto* q = static_cast<uint8_t*>(q_packed);
+  auto* sf = static_cast<uint8_t*>(s_ue4m3);
+  const auto* rb = static_cast<const uint8_t*>(rbits);
+  if (use_rht && rbits) nvfp4_quantize_kernel<true, true><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, rht_signs, rb);
+  else if (use_rht) nvfp4_quantize_kernel<true, false><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, rht_signs);
+  else if (rbits) nvfp4_quantize_kernel<false, true><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, 0u, rb);
+  else nvfp4_quantize_kernel<false, false><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax);
+  return launch_status();
+}
+
+mx_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t cols, void* q_row, void* s_row, void* q_col,
+                            void* s_col, float* gscale, void* workspace, void* stream) {
+  if (!nvfp4_args_ok(x, rows, cols, 128, q_row, s_row, gscale, workspace)) return MX_ERR_INVALID_ARG;
+  if (!q_col || !s_col || !aligned(q_col, 16) || !aligned(s_col, 16)) return MX_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  auto* amax = static_cast<unsigned int*>(workspace);
+  const auto* xb = static_cast<const uint16_t*>(x);
+  const mx_status p1 = nvfp4_pass1(xb, rows, cols, amax, false, 0u, st);
+  if (p1 != MX_OK) return p1;
+  dim3 grid;
+  if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_2d_kernel<<<grid, 256, 0, st>>>(xb, rows, cols, static_cast<uint8_t*>(q_row),
+                                                 static_cast<uint8_t*>(s_row), static_cast<uint8_t*>(q_col),
+                                                 static_cast<uint8_t*>(s_col), gscale, amax);
   return launch_status();
 }
 

@@ -510,21 +510,98 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
 }
 
 // ---------------------------------------------------------------------------------------------
+// NVFP4 training options ("Why FP8 training is stable" (magicnetworld.com), sec 13; "NVFP4: high
+// accuracy with 4 bits" (theluyuan.com), sec 3.2).
+// ---------------------------------------------------------------------------------------------
+// 16 bf16 values as FP32
+__device__ __forceinline__ void load_block16(const uint16_t* p, float (&f)[16]) {
+  const uint4 v0 = ld_stream_v4(p), v1 = ld_stream_v4(p + 8);
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+    f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+  }
+}
+
+// v <- 0.25 * H16 * (d .* v), d_i = -1 where bit i of `signs` is set; Sylvester butterflies in
+// the order h = 1, 2, 4, 8 (each sum rounded once in FP32), then an exact scaling by 1/4.
+__device__ __forceinline__ void fwht16(float (&v)[16], uint32_t signs) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((signs >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = __fadd_rn(a, b);
+        v[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+// E2M1 code of y by stochastic rounding with random byte r: for |y| < 6 between grid values
+// lo <= |y| < hi, round up iff r < floor(256 (|y| - lo) / (hi - lo)); |y| >= 6 gives 6.  Every
+// step is exact in FP32 (|y| - lo by Sterbenz, the step is a power of two).
+__device__ __forceinline__ uint32_t e2m1_stochastic(float y, uint32_t r) {
+  const uint32_t sign = (__float_as_uint(y) >> 31) << 3;
+  const float a = fabsf(y);
+  if (a >= 6.0f) return sign | 7u;
+  const int lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) + (a >= 4.0f);
+  const float lo_val = lo <= 4 ? 0.5f * lo : (lo == 5 ? 3.0f : 4.0f);
+  const float inv_step = lo < 4 ? 2.0f : (lo < 6 ? 1.0f : 0.5f);
+  const float t = floorf(__fmul_rn(__fmul_rn(__fsub_rn(a, lo_val), inv_step), 256.0f));
+  return sign | static_cast<uint32_t>(lo + (static_cast<float>(r) < t ? 1 : 0));
+}
+
+// E4M3 code of t = fl32(fl32(bamax / 6) / s_g): bamax * fl32(1/6) * rcp(s_g) is within 2^-21 of
+// t, so a +-2^-19 bracket that converts to one code decides it; otherwise the two IEEE quotients
+__device__ __forceinline__ uint32_t nv_block_scale_code(float bamax, float sg, float rsg) {
+  if (QuotientBracket::usable(sg)) {
+    const float y = __fmul_rn(__fmul_rn(bamax, 0.16666667163372040f), rsg);
+    const uint32_t c0 = cvt_e4m3x2(__fmul_rn(y, kBracketDown), 0.0f) & 0xFFu;
+    const uint32_t c1 = cvt_e4m3x2(__fmul_rn(y, kBracketUp), 0.0f) & 0xFFu;
+    if (c0 == c1) return c0;
+  }
+  return cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu;
+}
+
+// ---------------------------------------------------------------------------------------------
 // NVFP4 pass 1: global amax (as FP32 bits, atomicMax; non-negative floats order as integers).
 // ---------------------------------------------------------------------------------------------
+// RHT: the maximum is taken over the transformed values (every 1x16 block along a row), one block
+// (two 128-bit loads) per step.
+template <bool RHT = false>
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restrict__ x, int64_t n_vec8,
-                                                         unsigned int* __restrict__ amax_bits) {
+                                                         unsigned int* __restrict__ amax_bits, uint32_t signs = 0) {
   __shared__ uint32_t wmax[8];
-  uint32_t m = 0;
-  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n_vec8; i += static_cast<int64_t>(gridDim.x) * 256)
-    m = max(m, absmax_bits8(ld_stream_v4(x + i * 8)));
+  uint32_t m = 0;  // bf16 bits (RHT: FP32 bits) of the largest magnitude
+  if (RHT) {
+    for (int64_t i = blockIdx.x * 256ll + threadIdx.x; 2 * i < n_vec8; i += static_cast<int64_t>(gridDim.x) * 256) {
+      float f[16];
+      load_block16(x + i * 16, f);
+      fwht16(f, signs);
+      float a = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(f[k]));
+      m = max(m, __float_as_uint(a));
+    }
+  } else {
+    for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n_vec8; i += static_cast<int64_t>(gridDim.x) * 256)
+      m = max(m, absmax_bits8(ld_stream_v4(x + i * 8)));
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
-    atomicMax(amax_bits, m << 16);  // bf16 bits -> FP32 bits
+    atomicMax(amax_bits, RHT ? m : m << 16);  // as FP32 bits (non-negative floats order as integers)
   }
 }
 
@@ -538,11 +615,15 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-// NVFP4 pass 2.  CTA = 32 rows x 128 columns; thread = one 16-element block.
+// NVFP4 pass 2.  CTA = 32 rows x 128 columns; thread = one 16-element block.  RHT: the block is
+// transformed first (same signs as pass 1); SR: element codes by stochastic rounding of the IEEE
+// quotient with one random byte per element from rbits[rows][cols].
+template <bool RHT = false, bool SR = false>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                              int64_t cols, uint8_t* __restrict__ qp,
                                                              uint8_t* __restrict__ sf, float* __restrict__ gscale,
-                                                             const unsigned int* __restrict__ amax_bits) {
+                                                             const unsigned int* __restrict__ amax_bits,
+                                                             uint32_t signs = 0, const uint8_t* __restrict__ rbits = nullptr) {
   // grid: x = 32-row tile, y = 128-column tile; the last column tile may be half full
   // (cols % 128 == 64)
   __shared__ float s_glob[2];  // s_g and rcp(s_g), computed once per CTA
@@ -561,33 +642,50 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
   const int64_t c = tc * 128 + (t & 7) * 16;
   if (c >= cols) return;
 
-  const uint4 v0 = ld_stream_v4(x + r * cols + c);
-  const uint4 v1 = ld_stream_v4(x + r * cols + c + 8);
-  const uint32_t bm = max(absmax_bits8(v0), absmax_bits8(v1));
-  const float bamax = bf16_bits_to_float(bm);
-  // E4M3 code of t = fl32(fl32(bamax / 6) / s_g): bamax * fl32(1/6) * rcp(s_g) is within 2^-21 of
-  // t, so a +-2^-19 bracket that converts to one code decides it; otherwise the two IEEE quotients
-  uint32_t scode;
-  if (QuotientBracket::usable(sg)) {
-    const float y = __fmul_rn(__fmul_rn(bamax, 0.16666667163372040f), rsg);
-    const uint32_t c0 = cvt_e4m3x2(__fmul_rn(y, kBracketDown), 0.0f) & 0xFFu;
-    const uint32_t c1 = cvt_e4m3x2(__fmul_rn(y, kBracketUp), 0.0f) & 0xFFu;
-    scode = (c0 == c1) ? c0 : (cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu);
+  float f[16];
+  float bamax;
+  if (RHT) {
+    load_block16(x + r * cols + c, f);
+    fwht16(f, signs);
+    bamax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) bamax = fmaxf(bamax, fabsf(f[k]));
   } else {
-    scode = cvt_e4m3x2(__fdiv_rn(__fdiv_rn(bamax, 6.0f), sg), 0.0f) & 0xFFu;
-  }
-  const float s_hat = __fmul_rn(e4m3_to_float(scode), sg);
-  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  uint32_t lo = 0, hi = 0;
-  if (s_hat != 0.0f) {
-    const bool fast = QuotientBracket::usable(s_hat);
-    const QuotientBracket qb(fast ? s_hat : 1.0f);
+    const uint4 v0 = ld_stream_v4(x + r * cols + c);
+    const uint4 v1 = ld_stream_v4(x + r * cols + c + 8);
+    bamax = bf16_bits_to_float(max(absmax_bits8(v0), absmax_bits8(v1)));
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float a = bf16_bits_to_float(w[i] & 0xFFFFu), b = bf16_bits_to_float(w[i] >> 16);
-      const uint32_t byte = fast ? e2m1x2_quotient(a, b, qb) : cvt_e2m1x2(__fdiv_rn(a, s_hat), __fdiv_rn(b, s_hat));
-      if (i < 4) lo |= byte << (8 * i);
-      else hi |= byte << (8 * (i - 4));
+      f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+      f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+  }
+  const uint32_t scode = nv_block_scale_code(bamax, sg, rsg);
+  const float s_hat = __fmul_rn(e4m3_to_float(scode), sg);
+  uint32_t lo = 0, hi = 0;
+  if (s_hat != 0.0f) {
+    if (SR) {
+      const uint4 rb = *reinterpret_cast<const uint4*>(rbits + r * cols + c);
+      const uint32_t rw[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ra = (rw[i >> 1] >> (16 * (i & 1))) & 0xFFu, rb2 = (rw[i >> 1] >> (16 * (i & 1) + 8)) & 0xFFu;
+        const uint32_t byte = e2m1_stochastic(__fdiv_rn(f[2 * i], s_hat), ra) |
+                              (e2m1_stochastic(__fdiv_rn(f[2 * i + 1], s_hat), rb2) << 4);
+        if (i < 4) lo |= byte << (8 * i);
+        else hi |= byte << (8 * (i - 4));
+      }
+    } else {
+      const bool fast = QuotientBracket::usable(s_hat);
+      const QuotientBracket qb(fast ? s_hat : 1.0f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float a = f[2 * i], b = f[2 * i + 1];
+        const uint32_t byte = fast ? e2m1x2_quotient(a, b, qb) : cvt_e2m1x2(__fdiv_rn(a, s_hat), __fdiv_rn(b, s_hat));
+        if (i < 4) lo |= byte << (8 * i);
+        else hi |= byte << (8 * (i - 4));
+      }
     }
   }
   *reinterpret_cast<uint2*>(qp + r * (cols >> 1) + (c >> 1)) = make_uint2(lo, hi);
@@ -595,6 +693,128 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
   const int64_t chunk = (r >> 7) * (cols >> 6) + (c >> 6);
   sf[chunk * 512 + chunk_offset(static_cast<int>(r & 127), static_cast<int>((c >> 4) & 3))] =
       static_cast<uint8_t>(scode);
+}
+
+// NVFP4 with 16x16 2-D blocks (weights; "Why FP8 training is stable" (magicnetworld.com),
+// sec 13): one E4M3 scale per 16x16 block of x, so the row-wise copy and the transposed
+// (column-wise) copy hold the same codes and scales.  CTA = one 128 x 128 tile (8 x 8 blocks).
+// Pass 1 is nvfp4_amax_kernel<false>.  Outputs: q_row[rows][cols/2] packed, s_row in the NVFP4
+// GEMM layout of [rows][cols/16]; q_col[cols][rows/2], s_col the layout of [cols][rows/16].
+__global__ void __launch_bounds__(256) nvfp4_quantize_2d_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                int64_t cols, uint8_t* __restrict__ q_row,
+                                                                uint8_t* __restrict__ s_row,
+                                                                uint8_t* __restrict__ q_col,
+                                                                uint8_t* __restrict__ s_col, float* __restrict__ gscale,
+                                                                const unsigned int* __restrict__ amax_bits) {
+  __shared__ __align__(16) uint32_t tile[128 * 64];  // 128 rows x 128 bf16 (bf16x2 words)
+  __shared__ __align__(16) uint8_t srow[1024], scol[1024];
+  __shared__ uint32_t bmax[64];
+  __shared__ float shat[64];
+  __shared__ float s_glob[2];
+  const int64_t tr = blockIdx.x, tc = blockIdx.y;  // grid: x = row tile, y = column tile
+  const int t = threadIdx.x;
+  const int lc = t & 15, r0 = t >> 4;
+  if (t < 64) bmax[t] = 0;
+  if (t == 0) {
+    const float amax = __uint_as_float(*amax_bits);
+    const float g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    s_glob[0] = g;
+    s_glob[1] = rcp_approx(g);
+    if (tr == 0 && tc == 0) *gscale = g;
+  }
+  const uint16_t* xt = x + (tr * 128) * cols + tc * 128;
+  uint4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = ld_stream_v4(xt + static_cast<int64_t>(r0 + 16 * i) * cols + lc * 8);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(&tile[(r0 + 16 * i) * 64 + lc * 4]) = v[i];
+  __syncthreads();
+  // block (i, lc >> 1) holds this thread's row r0 + 16 i, columns lc * 8 .. + 7: combine the two
+  // lanes of a block's 16 columns and the warp's two rows, then the 8 warps in shared memory
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t m = absmax_bits8(v[i]);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    if ((t & 17) == 0) atomicMax(&bmax[i * 8 + (lc >> 1)], m);
+  }
+  __syncthreads();
+  const float sg = s_glob[0], rsg = s_glob[1];
+  if (t < 64) {  // block (t / 8, t % 8): scale code and s_hat
+    const uint32_t code = nv_block_scale_code(bf16_bits_to_float(bmax[t]), sg, rsg);
+    shat[t] = __fmul_rn(e4m3_to_float(code), sg);
+    bmax[t] = code;
+  }
+  __syncthreads();
+  // row-wise codes: 8 values of row r0 + 16 i per thread
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = r0 + 16 * i;
+    const float sh = shat[i * 8 + (lc >> 1)];
+    uint32_t packed = 0;
+    if (sh != 0.0f) {
+      const bool fast = QuotientBracket::usable(sh);
+      const QuotientBracket qb(fast ? sh : 1.0f);
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a = bf16_bits_to_float(w[k] & 0xFFFFu), b = bf16_bits_to_float(w[k] >> 16);
+        packed |= (fast ? e2m1x2_quotient(a, b, qb) : cvt_e2m1x2(__fdiv_rn(a, sh), __fdiv_rn(b, sh))) << (8 * k);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(q_row + (tr * 128 + r) * (cols >> 1) + tc * 64 + lc * 4) = packed;
+    if ((lc & 1) == 0) {  // block column b = lc / 2 -> chunk b / 4, byte (r, b % 4)
+      const int b = lc >> 1;
+      srow[(b >> 2) * 512 + chunk_offset(r, b & 3)] = static_cast<uint8_t>(bmax[i * 8 + b]);
+    }
+  }
+  // column-wise codes: 16 rows x 4 columns per thread, all inside block (2 rb + hb, cq / 4)
+  {
+    const int lane = t & 31;
+    const int hb = lane & 1;
+    const int cq = (lane >> 1) + 16 * ((t >> 5) & 1);
+    const int rb = t >> 6;
+    const int blk = (2 * rb + hb) * 8 + (cq >> 2);
+    const float sh = shat[blk];
+    uint2 u[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) u[r] = *reinterpret_cast<const uint2*>(&tile[(rb * 32 + hb * 16 + r) * 64 + 2 * cq]);
+    const bool fast = QuotientBracket::usable(sh);
+    const QuotientBracket qb(fast ? sh : 1.0f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 4 * cq + j;
+      const int sh16 = (j & 1) ? 16 : 0;
+      uint32_t w2[2] = {0, 0};
+      if (sh != 0.0f) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // rows 8h + 2k, 8h + 2k + 1 -> byte k
+            const int ra = 8 * h + 2 * k;
+            const float a = bf16_bits_to_float((((j < 2) ? u[ra].x : u[ra].y) >> sh16) & 0xFFFFu);
+            const float b = bf16_bits_to_float((((j < 2) ? u[ra + 1].x : u[ra + 1].y) >> sh16) & 0xFFFFu);
+            w2[h] |= (fast ? e2m1x2_quotient(a, b, qb) : cvt_e2m1x2(__fdiv_rn(a, sh), __fdiv_rn(b, sh))) << (8 * k);
+          }
+        }
+      }
+      *reinterpret_cast<uint2*>(q_col + (tc * 128 + c) * (rows >> 1) + tr * 64 + rb * 16 + hb * 8) =
+          make_uint2(w2[0], w2[1]);
+      const int bt = 2 * rb + hb;  // block index along the transposed row
+      scol[(bt >> 2) * 512 + chunk_offset(c, bt & 3)] = static_cast<uint8_t>(bmax[blk]);
+    }
+  }
+  __syncthreads();
+  // two scale chunks per copy: rows of this tile x 8 blocks of 16
+  if (t < 64) {
+    const int k = t >> 5, u = t & 31;
+    reinterpret_cast<uint4*>(s_row + (tr * (cols >> 6) + tc * 2 + k) * 512)[u] =
+        reinterpret_cast<const uint4*>(srow + k * 512)[u];
+  } else if (t < 128) {
+    const int k = (t - 64) >> 5, u = t & 31;
+    reinterpret_cast<uint4*>(s_col + (tc * (rows >> 6) + tr * 2 + k) * 512)[u] =
+        reinterpret_cast<const uint4*>(scol + k * 512)[u];
+  }
 }
 
 }  // namespace mxgb

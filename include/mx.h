@@ -144,6 +144,39 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea,
                   void* out, mx_out out_dtype, int64_t ldc, void* stream);
 
 /*
+ * nvfp4_quantize_ex -- NVFP4 with the training options of [DS] sec 13 and [NV] sec 3.2.
+ *
+ * Same arguments, layouts and limits as nvfp4_quantize, plus:
+ *   use_rht = 1: every 1x16 block along cols is first replaced by 0.25 * H16 * (d .* x), H16
+ *     the 16x16 Sylvester Hadamard matrix and d_i = -1 where bit i of rht_signs is set (the
+ *     random signs are an input; rht_signs <= 0xFFFF).  Computed in FP32 with butterflies in
+ *     the order h = 1, 2, 4, 8; the global maximum, block scales and codes are those of the
+ *     transformed values.  Operands transformed with the same signs multiply to the same
+ *     product (0.25 H16 is orthogonal and symmetric).
+ *   rbits != NULL: stochastic rounding of the element codes.  rbits[rows][cols] (u8, 16-byte
+ *     aligned) holds one random byte r per element; with y = fl32(x / s_hat), |y| < 6 lying
+ *     between E2M1 values lo <= |y| < hi, the code rounds up iff r < floor(256 (|y| - lo) /
+ *     (hi - lo)); |y| >= 6 gives 6.  NULL: round to nearest even as nvfp4_quantize.
+ * use_rht not 0/1 or rht_signs > 0xFFFF: MX_ERR_INVALID_ARG.
+ */
+mx_status nvfp4_quantize_ex(const void* x, int64_t rows, int64_t cols, int use_rht, uint32_t rht_signs,
+                            const void* rbits, void* q_packed, void* s_ue4m3, float* gscale, void* workspace,
+                            void* stream);
+
+/*
+ * nvfp4_quantize_2d -- NVFP4 with 16x16 2-D blocks (weights, [DS] sec 13).
+ *
+ * One E4M3 block scale per 16x16 block of x (the recipe of nvfp4_quantize with the block maximum
+ * over 256 elements; same global scale), written for both orientations: q_row[rows][cols/2] and
+ * s_row (the NVFP4 GEMM layout of [rows][cols/16]) as nvfp4_quantize writes them, and
+ * q_col[cols][rows/2], s_col (the layout of [cols][rows/16]) for the transposed matrix; the two
+ * hold the same codes and scales.  rows % 128 == 0, cols % 128 == 0; workspace as for
+ * nvfp4_quantize.
+ */
+mx_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t cols, void* q_row, void* s_row, void* q_col,
+                            void* s_col, float* gscale, void* workspace, void* stream);
+
+/*
  * mx_scales_from_fp32_blocks -- Float8BlockScaling scales in MX form.  [MX] sec 1.3.
  *
  * s: power-of-two FP32 block scales as mx_quantize(block = 128, sfmt = MX_SCALE_FP32_POW2)

@@ -82,6 +82,18 @@ def test_quantize_rejects_bad_arguments(lib):
     assert call(sfmt=4) == mx.MX_ERR_INVALID_ARG
 
 
+def test_nvfp4_option_entries_reject_bad_arguments(lib):
+    e = lib.nvfp4_quantize_ex
+    assert e(FAKE, 128, 128, 2, 0, None, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG   # use_rht
+    assert e(FAKE, 128, 128, 1, 0x10000, None, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert e(FAKE, 128, 128, 0, 0, FAKE + 4, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG  # rbits
+    assert e(FAKE, 128, 96, 0, 0, None, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    d = lib.nvfp4_quantize_2d
+    assert d(FAKE, 128, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG      # cols % 128
+    assert d(FAKE, 128, 128, FAKE, FAKE, None, FAKE, FAKE, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert d(FAKE, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_scale_conversion_rejects_bad_arguments(lib):
     c = lib.mx_scales_from_fp32_blocks
     assert c(None, 128, 128, 1, FAKE, None) == mx.MX_ERR_INVALID_ARG
