@@ -12,6 +12,8 @@ One step = one pass over every row of the hot path, each on its own seeded synth
 An extra group, not part of the default step, is measured with --only mx4:
   mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
        with the block scales in the MMA (FP32 out)
+  moe  grouped MXFP8 GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
+       in multiples of 128, one launch (bf16 out)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
        stochastic rounding (random bytes read from HBM), both, and 16x16 2-D blocks written in
        both orientations
@@ -49,6 +51,8 @@ F_LIN = 2 * 8192 * 4096 * 14336            # each of fprop / dgrad / wgrad
 F_NV = 2 * 8192 ** 3
 F_DS = 2 * 4096 * 7168 * 2048
 F_MX4 = 2 * 8192 ** 3
+MOE_SIZES = (3328, 1536, 2432, 1024, 2816, 1920, 2176, 1152)    # rows per expert, sum 16384
+F_MOE = 2 * sum(MOE_SIZES) * 14336 * 4096
 GEMM_FLOPS_STEP = 3 * F_LIN + F_NV + F_DS
 
 
@@ -176,6 +180,9 @@ class Workload:
             self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
         if "nvt" in groups:
             self.host["A8"] = synthetic.nvfp4_pair()[0]
+        if "moe" in groups:
+            self.host["A9"] = synthetic.normal(sum(MOE_SIZES), 4096, 1.0, 9000)
+            self.host["B9"] = synthetic.normal(len(MOE_SIZES) * 14336, 4096, 0.02, 9001)
         if "blk" in groups:
             self.host["A7"], self.host["B7"] = synthetic.deepseek_pair()
             self.host["W7"] = synthetic.mxfp8_linear()[1]
@@ -209,6 +216,15 @@ class Workload:
             self.Y5 = bf(4096, 2048)
             self.launches_per_step += 3
             self._outs += [self.Y5]
+        if "moe" in groups:
+            m9, n9 = sum(MOE_SIZES), len(MOE_SIZES) * 14336
+            self.A9q = (u8(m9, 4096), u8(sb(m9, 4096)))
+            self.B9q = (u8(n9, 4096), u8(sb(n9, 4096)))
+            self.off9 = torch.tensor([0] + list(__import__("itertools").accumulate(MOE_SIZES)), dtype=torch.int64,
+                                     device=dev)
+            self.Y9 = bf(m9, 14336)
+            self.launches_per_step += 1
+            self._outs += [self.Y9]
         if "nvt" in groups:
             g8 = torch.Generator(device="cpu").manual_seed(8100)
             self.R8 = torch.randint(0, 256, (8192, 8192), dtype=torch.uint8, generator=g8).to(dev)
@@ -271,6 +287,14 @@ class Workload:
             mark("dsgemm")
             mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
                                   out=self.Y5)
+        if "moe" in g:
+            if not getattr(self, "_moe_quantized", False):      # operands quantized once, outside the rows
+                mx.mx_quantize(d["A9"], layout=mx.ROWWISE, q_row=self.A9q[0], s_row=self.A9q[1])
+                mx.mx_quantize(d["B9"], layout=mx.ROWWISE, q_row=self.B9q[0], s_row=self.B9q[1])
+                self._moe_quantized = True
+            mark("moegemm")
+            mx.mx_gemm_grouped(self.A9q[0], self.A9q[1], mx.E4M3, self.B9q[0], self.B9q[1], mx.E4M3, self.off9,
+                               sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
         if "nvt" in g:
             q = self.A8q
             mark("nvq_rht")
@@ -309,7 +333,7 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm"]
 
 
 def row_report(name, ms, peaks):
@@ -326,7 +350,7 @@ def row_report(name, ms, peaks):
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
     f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS}[name]
+         "blkgemm": F_DS, "moegemm": F_MOE}[name]
     tf = f / s / 1e12
     peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
@@ -505,7 +529,7 @@ def main():
     ap.add_argument("--library-reference", action="store_true",
                     help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
-                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4, blk and nvt are measured only here) for profiling runs; "
+                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4, blk, nvt and moe are measured only here) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -585,7 +609,7 @@ def main():
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
     row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS}
+                 "blkgemm": F_DS, "moegemm": F_MOE}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
@@ -594,14 +618,14 @@ def main():
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
-               "nvfp4_quantize_2d": ["nvq_2d"]}
+               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2}
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -610,9 +634,9 @@ def main():
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks"):
+    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks", "mx_gemm_grouped"):
         flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
-                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS}[dom]
+                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE}[dom]
         fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm")
         peak = 3 * fp8_peak if fp4 else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12

@@ -8,7 +8,7 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
-  mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
+  mx_gemm_grouped, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
   nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
@@ -32,7 +32,7 @@ EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
-    "nvfp4_quantize_2d",
+    "nvfp4_quantize_2d", "mx_gemm_grouped",
 )
 
 
@@ -78,6 +78,7 @@ def load():
             "mx_scales_from_fp32_blocks": (i32, [vp, i64, i64, i32, vp, vp]),
             "nvfp4_quantize_ex": (i32, [vp, i64, i64, i32, ctypes.c_uint32, vp, vp, vp, vp, vp, vp]),
             "nvfp4_quantize_2d": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
+            "mx_gemm_grouped": (i32, [vp, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -284,6 +285,18 @@ def mx_gemm(qa, sa, ea, qb, sb, eb, M, N, K, out_dtype=OUT_BF16, out=None, strea
     st = load().mx_gemm(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, M, N, K, out.data_ptr(), out_dtype, ldc,
                         _stream(stream))
     _check(st, "mx_gemm")
+    return out
+
+
+def mx_gemm_grouped(qa, sa, ea, qb, sb, eb, group_offsets, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):
+    """MXFP8 grouped GEMM (include/mx.h, mx_gemm_grouped): rows off[g] .. off[g+1] of A times the
+    g-th [N][K] block of B.  group_offsets: int64 CUDA tensor [G + 1]."""
+    if group_offsets.dtype != torch.int64:
+        raise ValueError("group_offsets must be int64")
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().mx_gemm_grouped(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, _ptr(group_offsets),
+                                group_offsets.numel() - 1, M, N, K, out.data_ptr(), out_dtype, ldc, _stream(stream))
+    _check(st, "mx_gemm_grouped")
     return out
 
 

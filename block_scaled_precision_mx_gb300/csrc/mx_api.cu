@@ -154,21 +154,24 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
 }
 
 // Block-scaled CTA-pair kernel, 256 x 256 output tiles.
-template <int KIND, bool OUT_BF16>
-mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
+template <int KIND, bool OUT_BF16, bool GROUPED = false>
+mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st,
+                       int64_t b_rows = 0) {
   using Cfg = Gemm2Cfg<KIND>;
   static int max_clusters[64] = {};
   const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte scale chunks per 128 rows
   const int chunk_rows = Cfg::SF_CHUNK / 128;
   CUtensorMap ta, tb, tsa, tsb, tout;
   if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
-  if (!make_tmap(&tb, qb, args.N, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
+  const int64_t brows = GROUPED ? b_rows : args.N;  // grouped: the groups' B blocks stacked
+  if (!make_tmap(&tb, qb, brows, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
-  if (!make_tmap(&tsb, args.sfb, (args.N / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
+  if (!make_tmap(&tsb, args.sfb, (brows / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
   if (!make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)) return MX_ERR_CUDA;
-  const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
-  return launch_pairs(bs_gemm2_kernel<KIND, OUT_BF16>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters, st, ta,
-                      tb, tsa, tsb, tout, args);
+  // grouped: the tile count is known on the device only; every co-resident cluster runs
+  const int tiles = GROUPED ? 0x7FFFFFFF : (args.M / Cfg::BM) * (args.N / Cfg::BN);
+  return launch_pairs(bs_gemm2_kernel<KIND, OUT_BF16, GROUPED>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters,
+                      st, ta, tb, tsa, tsb, tout, args);
 }
 
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
@@ -377,6 +380,36 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
 }
 
+mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                          const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N, int64_t K, void* out,
+                          mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !out || !group_offsets) return MX_ERR_INVALID_ARG;
+  if (groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
+  if (groups * N > (1ll << 30)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16) ||
+      !aligned(group_offsets, 8))
+    return MX_ERR_INVALID_ARG;
+  if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
+    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
+    return MX_ERR_INVALID_ARG;
+  }
+  GemmArgs a{};
+  a.sfa = static_cast<const uint8_t*>(sa);
+  a.sfb = static_cast<const uint8_t*>(sb);
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.group_off = group_offsets;
+  a.groups = static_cast<int>(groups);
+  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
+  cudaStream_t st = as_stream(stream);
+  if (out_dtype == MX_OUT_BF16) return launch_gemm2<kMxf8, true, true>(qa, qb, K, a, st, groups * N);
+  return launch_gemm2<kMxf8, false, true>(qa, qb, K, a, st, groups * N);
+}
+
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols) {
   (void)rows;
   (void)cols;
@@ -526,7 +559,7 @@ mx_status mx_check(void* stream) {
   if (word) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_mx_error_word, &zero, sizeof(zero)) != cudaSuccess) return MX_ERR_CUDA;
-    return MX_ERR_TIMEOUT;
+    return (word & ~static_cast<unsigned int>(kSiteBadGroups)) ? MX_ERR_TIMEOUT : MX_ERR_INVALID_ARG;
   }
   return MX_OK;
 }

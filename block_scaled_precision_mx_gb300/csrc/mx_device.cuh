@@ -27,6 +27,7 @@ enum WaitSite : unsigned int {
   kSiteMmaTmemEmpty = 1u << 2,
   kSiteEpiTmemFull = 1u << 3,
   kSiteDrain = 1u << 4,
+  kSiteBadGroups = 1u << 5,  // not a wait: grouped GEMM offsets that break their contract
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

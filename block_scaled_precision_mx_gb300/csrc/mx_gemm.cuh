@@ -94,9 +94,13 @@ struct GemmArgs {
   const float* gb;
   void* out;
   int64_t ldc;
-  int M, N, K;  // K in elements
+  int M, N, K;  // K in elements (grouped: M = rows of all groups)
   uint32_t idesc;
+  const int64_t* group_off;  // grouped GEMM: device int64[groups + 1] row offsets of the groups
+  int groups;
 };
+
+constexpr int kMaxGroups = 1024;
 
 // Tile order: bands of 16 m-blocks; inside a band, m runs fastest, so the CTAs of one wave
 // share a few B tiles and a band of A tiles in L2.

@@ -100,7 +100,12 @@ struct Gemm2Cfg {
 
 // Scale tensors are read through 2-D byte tensor maps with 128-byte rows (a 512-byte scale chunk
 // is 4 such rows), so that the peer CTA's scale loads can complete on the leader's barrier too.
-template <int KIND, bool OUT_BF16>
+// GROUPED (MoE expert GEMMs in one launch; "MXFP8 on SM120: software support"
+// (xuesongtap.github.io), sec 1.2: grouped GEMM is its own entry point): group g multiplies rows
+// off[g] .. off[g+1] of A by the g-th [N][K] block of B into the same rows of C; tiles are
+// numbered group by group (the per-group tile counts' prefix sums sit in shared memory) and a
+// CTA whose 128 rows lie past its group's last row computes but stores nothing.
+template <int KIND, bool OUT_BF16, bool GROUPED = false>
 __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -133,8 +138,26 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
   const int nclusters = gridDim.x >> 1;
   const int num_mb = args.M / Cfg::BM;
   const int num_nb = args.N / Cfg::BN;
-  const int num_tiles = num_mb * num_nb;
   const int num_kt = args.K / Cfg::K_ELEMS;
+  __shared__ int grp_start[GROUPED ? kMaxGroups + 1 : 1];  // first tile of each group
+  if (GROUPED && threadIdx.x == 0) {
+    // offsets must start at 0, end at M, be multiples of 128 and never decrease; otherwise no
+    // tile runs and the error word reports it
+    const int64_t* off = args.group_off;
+    bool good = __ldg(off) == 0 && __ldg(off + args.groups) == args.M;
+    int t = 0;
+    for (int g = 0; g < args.groups; ++g) {
+      grp_start[g] = t;
+      const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
+      good = good && a >= 0 && b >= a && (a & 127) == 0 && (b & 127) == 0 && b <= args.M;
+      if (good) t += static_cast<int>((b - a + Cfg::BM - 1) / Cfg::BM) * num_nb;
+    }
+    if (!good) {
+      t = 0;
+      if (blockIdx.x == 0) atomicOr(&g_mx_error_word, kSiteBadGroups);
+    }
+    grp_start[args.groups] = t;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -162,6 +185,30 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
+  // tile -> (first A row, first B row, rows of A that belong to it, output column block)
+  auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb) {
+    int mb;
+    if (GROUPED) {
+      int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (grp_start[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+      }
+      const int64_t off = __ldg(args.group_off + lo), rows_g = __ldg(args.group_off + lo + 1) - off;
+      tile_coords(tile - grp_start[lo], static_cast<int>((rows_g + Cfg::BM - 1) / Cfg::BM), num_nb, mb, nb);
+      a_row0 = off + static_cast<int64_t>(mb) * Cfg::BM;
+      b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * Cfg::BN;
+      const int64_t left = rows_g - static_cast<int64_t>(mb) * Cfg::BM;
+      rows_valid = left < Cfg::BM ? static_cast<int>(left) : Cfg::BM;
+    } else {
+      tile_coords(tile, num_mb, num_nb, mb, nb);
+      a_row0 = static_cast<int64_t>(mb) * Cfg::BM;
+      b_row0 = static_cast<int64_t>(nb) * Cfg::BN;
+      rows_valid = Cfg::BM;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -172,10 +219,11 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte chunks per 128 rows
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-        int mb, nb;
-        tile_coords(tile, num_mb, num_nb, mb, nb);
-        const int a_row = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
-        const int b_row = nb * Cfg::BN + static_cast<int>(rank) * Cfg::ROWS;
+        int64_t a_row0, b_row0;
+        int rows_valid, nb;
+        decode(tile, a_row0, b_row0, rows_valid, nb);
+        const int a_row = static_cast<int>(a_row0) + static_cast<int>(rank) * Cfg::ROWS;
+        const int b_row = static_cast<int>(b_row0) + static_cast<int>(rank) * Cfg::ROWS;
         for (int kt = 0; kt < num_kt; ++kt) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, kSiteProducerEmpty)) {
             ok = false;
@@ -194,7 +242,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
 #pragma unroll
           for (int rc = 0; rc < 2; ++rc)
             tma_load_2d_pair(sSFB + stage * Cfg::SFB_BYTES + rc * Cfg::SF_CHUNK, &tmSFB, full_leader, 0,
-                             static_cast<int32_t>(((nb * 2 + rc) * kc + cfirst) * 4));
+                             static_cast<int32_t>(((b_row0 / 128 + rc) * kc + cfirst) * 4));
           ++issued;
           if (++stage == Cfg::STAGES) {
             stage = 0;
@@ -323,8 +371,10 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     if (KIND == kNvf4) gscale = __fmul_rn(*args.ga, *args.gb);
     uint32_t acc_it = 0;
     for (int tile = cluster; tile < num_tiles; tile += nclusters) {
-      int mb, nb;
-      tile_coords(tile, num_mb, num_nb, mb, nb);
+      int64_t a_row0, b_row0;
+      int rows_valid, nb;
+      decode(tile, a_row0, b_row0, rows_valid, nb);
+      const bool store = static_cast<int>(rank) * Cfg::ROWS < rows_valid;  // this CTA's rows exist
       bool ok = mbar_wait(tfull_bar, acc_it & 1, abort_flag, kSiteEpiTmemFull);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
@@ -340,7 +390,8 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       // each 32 x 32 chunk goes through this warp's swizzled staging buffer and one TMA store
       // (fewer, larger writes than per-thread vector stores, which slowed the MMA issue)
       uint8_t* buf = sOut + (warp - 2) * 4096;
-      const int32_t y0 = static_cast<int32_t>(mb * Cfg::BM + rank * Cfg::ROWS + q * 32);
+      const int32_t y0 = static_cast<int32_t>(a_row0 + rank * Cfg::ROWS + q * 32);
+      if (!store) continue;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float v[32];

@@ -191,6 +191,25 @@ mx_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t cols, void* q_r
 mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols, int block_rows, void* s_e8m0,
                                      void* stream);
 
+/*
+ * mx_gemm_grouped -- MXFP8 expert GEMMs of a mixture-of-experts layer in one launch.  [MX]
+ * sec 1.2 (grouped GEMM is its own entry point besides the single GEMMs).
+ *
+ * groups G (1..1024); group g multiplies rows off[g] .. off[g+1]-1 of A by the g-th block of B:
+ *   C[m][n] = sum_b sA[m][b] sB[gN + n][b] sum_{i<32} qA[m][32b+i] qB[gN + n][32b+i]
+ * for off[g] <= m < off[g+1], with the block scaling of mx_gemm.
+ * qa[M][K] (all groups' rows stacked), sa its E8M0 scales in the MX GEMM layout of [M][K];
+ * qb[G*N][K] (block g = rows gN .. gN+N-1), sb the layout of [G*N][K]; out M rows of ldc
+ * elements.  group_offsets: device int64[G + 1], 8-byte aligned, read by the kernel (so the
+ * expert sizes can come from device-side routing without a host round trip); they must satisfy
+ * off[0] = 0, off[G] = M, off[g] <= off[g+1] and off[g] % 128 == 0 (an empty group is allowed).
+ * Offsets that break this make the call do nothing and mx_check return MX_ERR_INVALID_ARG.
+ * M % 128 == 0, N % 256 == 0, K % 128 == 0, element formats as mx_gemm (MXFP8 only).
+ */
+mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                          const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N, int64_t K, void* out,
+                          mx_out out_dtype, int64_t ldc, void* stream);
+
 /* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
 
@@ -263,7 +282,8 @@ size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_
 /*
  * mx_check -- synchronizes `stream`, then reads and clears the library's device error word.
  * Returns MX_ERR_TIMEOUT if a kernel's bounded wait ran out since the last check,
- * MX_ERR_CUDA on a pending CUDA error, MX_OK otherwise.  This is the only call that
+ * MX_ERR_INVALID_ARG if the only event was a grouped GEMM whose device offsets broke their
+ * contract, MX_ERR_CUDA on a pending CUDA error, MX_OK otherwise.  This is the only call that
  * synchronizes.
  */
 mx_status mx_check(void* stream);

@@ -94,6 +94,24 @@ def test_nvfp4_option_entries_reject_bad_arguments(lib):
     assert d(FAKE, 128, 128, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == mx.MX_ERR_INVALID_ARG
 
 
+def test_grouped_gemm_rejects_bad_arguments(lib):
+    g = lib.mx_gemm_grouped
+    ok = [FAKE, FAKE, 0, FAKE, FAKE, 0, FAKE, 2, 512, 512, 256, FAKE, 1, 512, None]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return g(*a)
+    assert call(a6=None) == mx.MX_ERR_INVALID_ARG          # no offsets
+    assert call(a7=0) == mx.MX_ERR_INVALID_ARG             # no groups
+    assert call(a7=1025) == mx.MX_ERR_INVALID_ARG
+    assert call(a9=384) == mx.MX_ERR_INVALID_ARG           # N % 256
+    assert call(a6=FAKE + 4) == mx.MX_ERR_INVALID_ARG      # offsets alignment
+    assert call(a2=2) == mx.MX_ERR_UNSUPPORTED             # MXFP4 operands
+    assert call(a2=9) == mx.MX_ERR_INVALID_ARG
+
+
 def test_scale_conversion_rejects_bad_arguments(lib):
     c = lib.mx_scales_from_fp32_blocks
     assert c(None, 128, 128, 1, FAKE, None) == mx.MX_ERR_INVALID_ARG

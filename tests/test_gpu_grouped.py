@@ -1,0 +1,94 @@
+"""GPU parity of the grouped MXFP8 GEMM (mixture-of-experts expert products in one launch; "MXFP8
+on SM120: software support" (xuesongtap.github.io), sec 1.2) against the CPU oracle, group by
+group: rows off[g] .. off[g+1] of A times the g-th [N][K] block of B, within |y - y_ref| <=
+1e-5 * sum_k |a_k b_k| (+ one bf16 ulp for bf16 output).  Covers groups whose rows end in half
+a 256-row tile, empty groups, one group equal to the plain GEMM, and offsets that break the
+contract (no work, MX_ERR_INVALID_ARG from mx_check).
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_precision_mx_gb300 as mx
+import oracle as orc
+from tests.layouts import chunked_to_plain, plain_to_chunked
+from tests.test_gpu_gemm import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def random_operands(M, G, N, K, seed):
+    rng = np.random.default_rng(seed)
+    sign = lambda shape: rng.integers(0, 2, shape, dtype=np.uint8) << 7
+    qa = rng.integers(0, 0x7E, (M, K), dtype=np.uint8) | sign((M, K))
+    qb = rng.integers(0, 0x7E, (G * N, K), dtype=np.uint8) | sign((G * N, K))
+    sa = rng.integers(118, 136, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(118, 136, (G * N, K // 32), dtype=np.uint8)
+    return qa, sa, qb, sb
+
+
+def run_grouped(sizes, N, K, out_dtype, seed, sample=None):
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    qa, sa, qb, sb = random_operands(M, G, N, K, seed)
+    y = mx.mx_gemm_grouped(dev(qa), dev(plain_to_chunked(sa)), mx.E4M3, dev(qb), dev(plain_to_chunked(sb)), mx.E4M3,
+                           dev(off), M, N, K, out_dtype=out_dtype)
+    assert mx.mx_check() == mx.MX_OK
+    yn = y.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        rows = np.arange(hi - lo) if sample is None else np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64))
+        ref, ab = orc.mx_gemm(qa[lo:hi], sa[lo:hi], orc.E4M3, qb[g * N:(g + 1) * N], sb[g * N:(g + 1) * N], orc.E4M3,
+                              rows=rows)
+        assert_close(yn[lo + rows], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"group {g}")
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_grouped_half_tiles_and_empty_groups(out_dtype):
+    run_grouped([256, 128, 0, 384], 512, 512, out_dtype, seed=1)
+
+
+def test_grouped_many_groups_moe_shape():
+    rng = np.random.default_rng(2)
+    sizes = (rng.integers(0, 9, 16) * 128).tolist()           # 16 experts, 0 .. 1024 rows each
+    run_grouped(sizes, 1024, 2048, mx.OUT_BF16, seed=3, sample=24)
+
+
+def test_single_group_equals_plain_gemm():
+    M, N, K = 512, 768, 1024
+    qa, sa, qb, sb = random_operands(M, 1, N, K, 4)
+    args = (dev(qa), dev(plain_to_chunked(sa)), mx.E4M3, dev(qb), dev(plain_to_chunked(sb)), mx.E4M3)
+    y1 = mx.mx_gemm(*args, M, N, K, out_dtype=mx.OUT_F32)
+    y2 = mx.mx_gemm_grouped(*args, dev(np.array([0, M], np.int64)), M, N, K, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("off", [[0, 100, 256], [0, 384, 256], [128, 256, 512], [0, 256, 384]])
+def test_grouped_rejects_broken_offsets_on_the_device(off):
+    # not a multiple of 128, decreasing, not starting at 0, not ending at M (= 512): no tile runs
+    M, N, K = 512, 256, 256
+    qa, sa, qb, sb = random_operands(M, 2, N, K, 5)
+    out = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    st = mx.load().mx_gemm_grouped(dev(qa).data_ptr(), dev(plain_to_chunked(sa)).data_ptr(), mx.E4M3,
+                                   dev(qb).data_ptr(), dev(plain_to_chunked(sb)).data_ptr(), mx.E4M3,
+                                   dev(np.array(off, np.int64)).data_ptr(), 2, M, N, K, out.data_ptr(), mx.OUT_F32, N,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == mx.MX_OK                          # the host cannot see device offsets
+    assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
+    assert bool((out == 7.0).all())
+    assert mx.mx_check() == mx.MX_OK               # the error word was cleared
