@@ -80,6 +80,7 @@ def _load():
                 "orc_e2m1_stochastic": (ctypes.c_uint8, [f32, ctypes.c_uint8]),
                 "orc_nv_quantize_ex": (None, [p, i64, i64, i32, u32, p, p, p, ctypes.POINTER(f32)]),
                 "orc_nv_quantize_2d16": (None, [p, i64, i64, p, p, ctypes.POINTER(f32)]),
+                "orc_mx_quantize_rowwise_f32": (None, [p, i64, i64, i32, p, p]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -140,6 +141,16 @@ def mx_quantize_rowwise(x, fmt: int):
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 32), np.uint8)
     _load().orc_mx_quantize_rowwise(_ptr(xb), rows, cols, fmt, _ptr(q), _ptr(s))
+    return q, s
+
+
+def mx_quantize_rowwise_f32(x, fmt: int):
+    """Row-wise MX quantization of FP32 values x[rows][cols]: (q, s [rows][cols/32])."""
+    xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    rows, cols = xf.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty((rows, cols // 32), np.uint8)
+    _load().orc_mx_quantize_rowwise_f32(_ptr(xf), rows, cols, fmt, _ptr(q), _ptr(s))
     return q, s
 
 

@@ -264,6 +264,34 @@ void orc_mx_quantize_colwise(const uint16_t* x, int64_t rows, int64_t cols, int 
                      sT + c * nb + b);
 }
 
+/* row-wise MX quantization of FP32 values (a GEMM's FP32 results quantized
+   for the next product): the rule of mx_block on float input.
+   x[rows][cols] float -> q[rows][cols], s[rows][cols/32] (plain layout) */
+void orc_mx_quantize_rowwise_f32(const float* x, int64_t rows, int64_t cols, int fmt,
+                                 uint8_t* q, uint8_t* s) {
+    int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* xb = x + r * cols + b * 32;
+            double amax = 0.0; int bad = 0;
+            for (int i = 0; i < 32; ++i) {
+                double v = (double)xb[i];
+                if (!isfinite(v)) bad = 1;
+                else if (fabs(v) > amax) amax = fabs(v);
+            }
+            if (bad) {
+                s[r * nb + b] = 0xFF;
+                for (int i = 0; i < 32; ++i) q[r * cols + b * 32 + i] = (uint8_t)((fmt == FMT_E2M1) ? 0x7 : 0x7F);
+                continue;
+            }
+            int k = orc_mx_scale_exp(amax, fmt);
+            s[r * nb + b] = (uint8_t)(k + 127);
+            for (int i = 0; i < 32; ++i)
+                q[r * cols + b * 32 + i] = (uint8_t)orc_encode(fmt, ldexp((double)xb[i], -k));
+        }
+}
+
 /* ---------------------------------------------------------------------- */
 /* DeepSeek fine-grained FP8 quantization, [DS] sec 4 and sec 5           */
 /* s = fl32(amax / 448), q = E4M3(fl32(x / s))                             */

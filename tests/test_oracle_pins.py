@@ -389,3 +389,32 @@ def test_ds_gemm_tracks_fp64_of_unquantized_inputs():
     rel = np.abs(y - ref) / absref
     assert rel.max() < 2.0 ** -4          # per-product relative error <= 2^-4 bounds the sum
     assert np.median(rel) < 5e-3
+
+
+# ------------------------------------------------------------------ MX quantization of FP32 values
+def test_mx_rowwise_f32_equals_bf16_path_on_bf16_values():
+    g = torch.Generator().manual_seed(13)
+    x = (torch.randn(64, 256, generator=g) * torch.logspace(-9, 9, 256)).to(torch.bfloat16)
+    for fmt in (E4M3, E5M2):
+        q1, s1 = orc.mx_quantize_rowwise(bits(x), fmt)
+        q2, s2 = orc.mx_quantize_rowwise_f32(x.float().numpy(), fmt)
+        assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+
+
+def test_mx_rowwise_f32_full_mantissa_matches_bruteforce():
+    # FP32 values with 24-bit mantissas (not bf16): scale by the floor rule, codes by a scan
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((8, 128)) * np.exp2(rng.integers(-30, 30, (8, 128)))).astype(np.float32)
+    x[3, 40] = np.inf
+    q, s = orc.mx_quantize_rowwise_f32(x, E4M3)
+    for r in range(8):
+        for b in range(4):
+            blk = x[r, 32 * b:32 * b + 32].astype(np.float64)
+            if not np.isfinite(blk).all():
+                assert s[r, b] == 0xFF and (q[r, 32 * b:32 * b + 32] == 0x7F).all()
+                continue
+            k = math.frexp(np.abs(blk).max())[1] - 1 - 8
+            k = max(k, -127)
+            assert s[r, b] == 127 + k
+            for i in range(32):
+                assert q[r, 32 * b + i] == orc.encode_bruteforce(E4M3, math.ldexp(float(blk[i]), -k))
