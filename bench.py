@@ -12,6 +12,8 @@ One step = one pass over every row of the hot path, each on its own seeded synth
 An extra group, not part of the default step, is measured with --only mx4:
   mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
        with the block scales in the MMA (FP32 out)
+  fuse fprop 8192x4096x14336 with the MX (E4M3) quantization of Y fused into the GEMM epilogue,
+       against the unfused pair (bf16 fprop, then row-wise MX quantize of Y)
   moe  grouped MXFP8 GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
        in multiples of 128, one launch (bf16 out)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
@@ -180,6 +182,8 @@ class Workload:
             self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
         if "nvt" in groups:
             self.host["A8"] = synthetic.nvfp4_pair()[0]
+        if "fuse" in groups:
+            self.host["X10"], self.host["W10"], _ = synthetic.mxfp8_linear()
         if "moe" in groups:
             self.host["A9"] = synthetic.normal(sum(MOE_SIZES), 4096, 1.0, 9000)
             self.host["B9"] = synthetic.normal(len(MOE_SIZES) * 14336, 4096, 0.02, 9001)
@@ -216,6 +220,13 @@ class Workload:
             self.Y5 = bf(4096, 2048)
             self.launches_per_step += 3
             self._outs += [self.Y5]
+        if "fuse" in groups:
+            self.X10q = (u8(8192, 4096), u8(sb(8192, 4096)))
+            self.W10q = (u8(14336, 4096), u8(sb(14336, 4096)))
+            self.Y10q = (u8(8192, 14336), u8(sb(8192, 14336)))
+            self.Y10 = bf(8192, 14336)
+            self.launches_per_step += 3
+            self._outs += [self.Y10q[0]]
         if "moe" in groups:
             m9, n9 = sum(MOE_SIZES), len(MOE_SIZES) * 14336
             self.A9q = (u8(m9, 4096), u8(sb(m9, 4096)))
@@ -287,6 +298,18 @@ class Workload:
             mark("dsgemm")
             mx.fp8_blockwise_gemm(self.A5q[0], self.A5q[1], self.B5q[0], self.B5q[1], 4096, 2048, 7168, mx.OUT_BF16,
                                   out=self.Y5)
+        if "fuse" in g:
+            if not getattr(self, "_fuse_quantized", False):     # operands quantized once, outside the rows
+                mx.mx_quantize(d["X10"], layout=mx.ROWWISE, q_row=self.X10q[0], s_row=self.X10q[1])
+                mx.mx_quantize(d["W10"], layout=mx.ROWWISE, q_row=self.W10q[0], s_row=self.W10q[1])
+                self._fuse_quantized = True
+            mark("fusedgemm")
+            mx.mx_gemm_mxout(self.X10q[0], self.X10q[1], mx.E4M3, self.W10q[0], self.W10q[1], mx.E4M3, 8192, 14336,
+                             4096, q_out=self.Y10q[0], s_out=self.Y10q[1])
+            mark("unfused")
+            mx.mx_gemm(self.X10q[0], self.X10q[1], mx.E4M3, self.W10q[0], self.W10q[1], mx.E4M3, 8192, 14336, 4096,
+                       mx.OUT_BF16, out=self.Y10)
+            mx.mx_quantize(self.Y10, layout=mx.ROWWISE, q_row=self.Y10q[0], s_row=self.Y10q[1])
         if "moe" in g:
             if not getattr(self, "_moe_quantized", False):      # operands quantized once, outside the rows
                 mx.mx_quantize(d["A9"], layout=mx.ROWWISE, q_row=self.A9q[0], s_row=self.A9q[1])
@@ -333,7 +356,7 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "fusedgemm", "unfused"]
 
 
 def row_report(name, ms, peaks):
@@ -350,7 +373,7 @@ def row_report(name, ms, peaks):
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
     f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS, "moegemm": F_MOE}[name]
+         "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "unfused": F_LIN}[name]
     tf = f / s / 1e12
     peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
@@ -529,7 +552,7 @@ def main():
     ap.add_argument("--library-reference", action="store_true",
                     help="print cuBLASLt reference throughputs for the GEMM shapes (context only)")
     ap.add_argument("--only", default=None,
-                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4, blk, nvt and moe are measured only here) for profiling runs; "
+                    help="comma-separated subset of row groups (q2, lin, nv, ds; mx4, blk, nvt, moe and fuse are measured only here) for profiling runs; "
                          "a line printed with --only is not a bench value")
     args = ap.parse_args()
     if args.impl == "reference":
@@ -609,7 +632,7 @@ def main():
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
     row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS, "moegemm": F_MOE}
+                 "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
@@ -618,14 +641,16 @@ def main():
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
-               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"]}
+               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "mx_gemm_mxout": ["fusedgemm"],
+               "mx_gemm_then_quantize": ["unfused"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1}
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "mx_gemm_mxout": 1,
+                "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
     traffic = None
@@ -634,9 +659,11 @@ def main():
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks", "mx_gemm_grouped"):
+    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks", "mx_gemm_grouped",
+               "mx_gemm_mxout", "mx_gemm_then_quantize"):
         flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
-                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE}[dom]
+                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE, "mx_gemm_mxout": F_LIN,
+                 "mx_gemm_then_quantize": F_LIN}[dom]
         fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm")
         peak = 3 * fp8_peak if fp4 else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12

@@ -8,7 +8,7 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
-  mx_gemm_grouped, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
+  mx_gemm_grouped, mx_gemm_mxout, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
   nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
@@ -32,7 +32,7 @@ EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
-    "nvfp4_quantize_2d", "mx_gemm_grouped",
+    "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout",
 )
 
 
@@ -79,6 +79,7 @@ def load():
             "nvfp4_quantize_ex": (i32, [vp, i64, i64, i32, ctypes.c_uint32, vp, vp, vp, vp, vp, vp]),
             "nvfp4_quantize_2d": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
             "mx_gemm_grouped": (i32, [vp, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
+            "mx_gemm_mxout": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, vp, i64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -286,6 +287,20 @@ def mx_gemm(qa, sa, ea, qb, sb, eb, M, N, K, out_dtype=OUT_BF16, out=None, strea
                         _stream(stream))
     _check(st, "mx_gemm")
     return out
+
+
+def mx_gemm_mxout(qa, sa, ea, qb, sb, eb, M, N, K, out_elem=E4M3, q_out=None, s_out=None, stream=None):
+    """MXFP8 GEMM with the MX quantization of its results fused into the epilogue (include/mx.h,
+    mx_gemm_mxout).  Returns (q_out [M][N] u8 codes, s_out flat u8 scales in the MX GEMM layout)."""
+    dev = qa.device
+    if q_out is None:
+        q_out = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    if s_out is None:
+        s_out = _u8(M * N // 32, dev)
+    st = load().mx_gemm_mxout(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, M, N, K, out_elem, _ptr(q_out),
+                              _ptr(s_out), q_out.stride(0), _stream(stream))
+    _check(st, "mx_gemm_mxout")
+    return q_out, s_out
 
 
 def mx_gemm_grouped(qa, sa, ea, qb, sb, eb, group_offsets, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):

@@ -154,7 +154,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
 }
 
 // Block-scaled CTA-pair kernel, 256 x 256 output tiles.
-template <int KIND, bool OUT_BF16, bool GROUPED = false>
+template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st,
                        int64_t b_rows = 0) {
   using Cfg = Gemm2Cfg<KIND>;
@@ -167,11 +167,15 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
   if (!make_tmap(&tb, qb, brows, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
   if (!make_tmap(&tsb, args.sfb, (brows / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
-  if (!make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)) return MX_ERR_CUDA;
+  // (MX output: the epilogue stores codes itself; the map describes the code buffer as FP32
+  // words and is never used)
+  const bool ok_out = MXOUT >= 0 ? make_out_tmap(&tout, args.q_out, args.M, args.N / 4, args.ldc / 4, false)
+                                 : make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16);
+  if (!ok_out) return MX_ERR_CUDA;
   // grouped: the tile count is known on the device only; every co-resident cluster runs
   const int tiles = GROUPED ? 0x7FFFFFFF : (args.M / Cfg::BM) * (args.N / Cfg::BN);
-  return launch_pairs(bs_gemm2_kernel<KIND, OUT_BF16, GROUPED>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters,
-                      st, ta, tb, tsa, tsb, tout, args);
+  return launch_pairs(bs_gemm2_kernel<KIND, OUT_BF16, GROUPED, MXOUT>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles,
+                      max_clusters, st, ta, tb, tsa, tsb, tout, args);
 }
 
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
@@ -378,6 +382,35 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 128, bn256 ? 256 : 128, 1);
   if (bn256) return bf ? launch_gemm<kMxf8, 256, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 256, false>(qa, qb, K, a, st);
   return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
+}
+
+mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                        int64_t M, int64_t N, int64_t K, mx_elem out_elem, void* q_out, void* s_out, int64_t ldq,
+                        void* stream) {
+  if (!qa || !sa || !qb || !sb || !q_out || !s_out) return MX_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return MX_ERR_INVALID_ARG;
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || ldq < N || ldq % 16) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(q_out, 16) ||
+      !aligned(s_out, 16))
+    return MX_ERR_INVALID_ARG;
+  if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
+    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
+    return MX_ERR_INVALID_ARG;
+  }
+  if (out_elem != MX_E4M3 && out_elem != MX_E5M2) return out_elem == MX_E2M1 ? MX_ERR_UNSUPPORTED : MX_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.sfa = static_cast<const uint8_t*>(sa);
+  a.sfb = static_cast<const uint8_t*>(sb);
+  a.q_out = static_cast<uint8_t*>(q_out);
+  a.s_out = static_cast<uint8_t*>(s_out);
+  a.ldc = ldq;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
+  cudaStream_t st = as_stream(stream);
+  if (out_elem == MX_E4M3) return launch_gemm2<kMxf8, false, false, 0>(qa, qb, K, a, st);
+  return launch_gemm2<kMxf8, false, false, 1>(qa, qb, K, a, st);
 }
 
 mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,

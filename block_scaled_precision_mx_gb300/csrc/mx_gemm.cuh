@@ -98,6 +98,8 @@ struct GemmArgs {
   uint32_t idesc;
   const int64_t* group_off;  // grouped GEMM: device int64[groups + 1] row offsets of the groups
   int groups;
+  uint8_t* q_out;  // MX output: codes [M][ldc bytes] and E8M0 scales in the MX GEMM layout
+  uint8_t* s_out;
 };
 
 constexpr int kMaxGroups = 1024;

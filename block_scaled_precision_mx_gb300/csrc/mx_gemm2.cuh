@@ -59,6 +59,9 @@ __device__ __forceinline__ void store_chunk_32x32(const CUtensorMap* tmOut, uint
   }
 }
 
+// byte offset of row i's 4 scale bytes inside a 512-byte MX scale chunk
+__device__ __forceinline__ int chunk_offset_mx(int i) { return (i & 31) * 16 + (i >> 5) * 4; }
+
 template <int KIND>
 struct Gemm2Cfg {
   static constexpr int BM = 256;       // rows per pair tile (128 per CTA)
@@ -105,7 +108,12 @@ struct Gemm2Cfg {
 // off[g] .. off[g+1] of A by the g-th [N][K] block of B into the same rows of C; tiles are
 // numbered group by group (the per-group tile counts' prefix sums sit in shared memory) and a
 // CTA whose 128 rows lie past its group's last row computes but stores nothing.
-template <int KIND, bool OUT_BF16, bool GROUPED = false>
+// MXOUT >= 0 (0 = E4M3, 1 = E5M2): the epilogue quantizes its FP32 results itself, row-wise in
+// 1x32 blocks with the MX rule, and writes codes and E8M0 scales (in the layout the next MX
+// product reads as its A operand) instead of bf16 / FP32 values -- the producer-side fusion of
+// the next layer's quantization ("Why FP8 training is stable" (magicnetworld.com), sec 9: the
+// activations feeding the next FP8 product are quantized before they leave).
+template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -392,6 +400,46 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
       uint8_t* buf = sOut + (warp - 2) * 4096;
       const int32_t y0 = static_cast<int32_t>(a_row0 + rank * Cfg::ROWS + q * 32);
       if (!store) continue;
+      if constexpr (MXOUT >= 0) {
+        // this thread's row holds 4 whole 1x32 blocks (its 128 columns): amax, E8M0 byte
+        // max(exp(amax) - emax, 0) (0xFF with codes 0x7F for Inf / NaN), codes of x * 2^-k
+        constexpr int kEmax = (MXOUT == 0) ? 8 : 15;
+        const int64_t row = y0 + lane;
+        const int64_t col0 = static_cast<int64_t>(nb) * Cfg::BN + half * HALF;
+        uint32_t sbytes = 0;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          uint32_t m = 0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) m = max(m, r[c][i] & 0x7FFFFFFFu);
+          uint32_t sb, w[8];
+          if (m >= 0x7F800000u) {
+            sb = 0xFF;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = 0x7F7F7F7Fu;
+          } else {
+            const int e = static_cast<int>(m >> 23);
+            sb = e > kEmax ? static_cast<uint32_t>(e - kEmax) : 0u;
+            const float inv = __uint_as_float((254u - sb) << 23);  // 2^-(sb - 127), always normal
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float f0 = __fmul_rn(__uint_as_float(r[c][4 * k]), inv);
+              const float f1 = __fmul_rn(__uint_as_float(r[c][4 * k + 1]), inv);
+              const float f2 = __fmul_rn(__uint_as_float(r[c][4 * k + 2]), inv);
+              const float f3 = __fmul_rn(__uint_as_float(r[c][4 * k + 3]), inv);
+              w[k] = (MXOUT == 0) ? (cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16))
+                                  : (cvt_e5m2x2(f0, f1) | (cvt_e5m2x2(f2, f3) << 16));
+            }
+          }
+          uint4* dst = reinterpret_cast<uint4*>(args.q_out + row * args.ldc + col0 + c * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          sbytes |= sb << (8 * c);
+        }
+        // chunk (row / 128, 128-column block of this half) of the [M][N/32] scales
+        *reinterpret_cast<uint32_t*>(args.s_out + ((row >> 7) * (args.N >> 7) + (col0 >> 7)) * 512 +
+                                     chunk_offset_mx(static_cast<int>(row & 127))) = sbytes;
+      } else {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         float v[32];
@@ -399,6 +447,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND>::THREADS, 1)
         for (int i = 0; i < 32; ++i)
           v[i] = (KIND == kNvf4) ? __fmul_rn(__uint_as_float(r[c][i]), gscale) : __uint_as_float(r[c][i]);
         store_chunk_32x32<OUT_BF16>(&tmOut, buf, v, lane, static_cast<int32_t>(nb * Cfg::BN + half * HALF + c * 32), y0);
+      }
       }
     }
   }

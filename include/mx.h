@@ -192,6 +192,22 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
                                      void* stream);
 
 /*
+ * mx_gemm_mxout -- MXFP8 GEMM whose epilogue quantizes its own results for the next product
+ * (producer-side fusion of the MX quantization; [MX] sec 0.1 rule, [DS] sec 9 quantizes the
+ * activations that feed the next FP8 product before they leave).
+ *
+ * The product of mx_gemm (same operands, formats and FP32 accumulation), then per 1x32 block of
+ * each output row the MX quantization of the FP32 results into out_elem (MX_E4M3 or MX_E5M2):
+ * scale byte max(exp(amax) - emax, 0) (0xFF and codes 0x7F when a result is Inf or NaN), codes
+ * RNE-satfinite(y * 2^-k).  q_out[M][ldq] u8 codes (ldq >= N, ldq % 16 == 0), s_out: M*N/32
+ * bytes in the MX GEMM layout of [M][N] -- exactly the A operand of a following mx_gemm.
+ * No bf16 / FP32 output is written.  M % 256 == 0, N % 256 == 0, K % 128 == 0.
+ */
+mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                        int64_t M, int64_t N, int64_t K, mx_elem out_elem, void* q_out, void* s_out, int64_t ldq,
+                        void* stream);
+
+/*
  * mx_gemm_grouped -- MXFP8 expert GEMMs of a mixture-of-experts layer in one launch.  [MX]
  * sec 1.2 (grouped GEMM is its own entry point besides the single GEMMs).
  *

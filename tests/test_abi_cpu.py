@@ -112,6 +112,15 @@ def test_grouped_gemm_rejects_bad_arguments(lib):
     assert call(a2=9) == mx.MX_ERR_INVALID_ARG
 
 
+def test_fused_output_gemm_rejects_bad_arguments(lib):
+    f = lib.mx_gemm_mxout
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 0, 128, 256, 256, 0, FAKE, FAKE, 256, None) == mx.MX_ERR_INVALID_ARG  # M % 256
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 256, 256, 0, FAKE, FAKE, 128, None) == mx.MX_ERR_INVALID_ARG  # ldq < N
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 256, 256, 0, None, FAKE, 256, None) == mx.MX_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 256, 256, 2, FAKE, FAKE, 256, None) == mx.MX_ERR_UNSUPPORTED  # E2M1 out
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 0, 256, 256, 256, 5, FAKE, FAKE, 256, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_scale_conversion_rejects_bad_arguments(lib):
     c = lib.mx_scales_from_fp32_blocks
     assert c(None, 128, 128, 1, FAKE, None) == mx.MX_ERR_INVALID_ARG
