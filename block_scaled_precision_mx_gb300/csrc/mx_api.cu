@@ -157,7 +157,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
 template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st,
                        int64_t b_rows = 0) {
-  using Cfg = Gemm2Cfg<KIND>;
+  using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>;
   static int max_clusters[64] = {};
   const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte scale chunks per 128 rows
   const int chunk_rows = Cfg::SF_CHUNK / 128;
