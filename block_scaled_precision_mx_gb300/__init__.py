@@ -32,7 +32,7 @@ EXPORTS = (
     "mx_abi_version", "mx_status_string", "mx_quantize", "mx_gemm", "nvfp4_workspace_bytes",
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
-    "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout",
+    "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
 )
 
 
@@ -80,6 +80,8 @@ def load():
             "nvfp4_quantize_2d": (i32, [vp, i64, i64, vp, vp, vp, vp, vp, vp, vp]),
             "mx_gemm_grouped": (i32, [vp, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
             "mx_gemm_mxout": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, vp, i64, vp]),
+            "mx_unswizzle_scales": (i32, [vp, i64, i64, vp, vp]),
+            "mx_swizzle_scales": (i32, [vp, i64, i64, vp, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -179,6 +181,28 @@ def mx_scales_from_fp32_blocks(s: torch.Tensor, rows: int, cols: int, block_rows
         out = _u8(rows * cols // 32, s.device)
     st = load().mx_scales_from_fp32_blocks(_ptr(s), rows, cols, block_rows, _ptr(out), _stream(stream))
     _check(st, "mx_scales_from_fp32_blocks")
+    return out
+
+
+def mx_unswizzle_scales(s: torch.Tensor, rows: int, nblocks: int, out=None, stream=None):
+    """GEMM-layout scale bytes -> plain uint8 [rows][nblocks] (include/mx.h, mx_unswizzle_scales);
+    nblocks = K/32 for MX scales, K/16 for NVFP4 scales."""
+    if s.dtype != torch.uint8:
+        raise ValueError("s must be uint8")
+    if out is None:
+        out = torch.empty(rows, nblocks, dtype=torch.uint8, device=s.device)
+    _check(load().mx_unswizzle_scales(_ptr(s), rows, nblocks, _ptr(out), _stream(stream)), "mx_unswizzle_scales")
+    return out
+
+
+def mx_swizzle_scales(plain: torch.Tensor, out=None, stream=None):
+    """plain uint8 [rows][nblocks] -> GEMM-layout scale bytes, flat (include/mx.h, mx_swizzle_scales)."""
+    if plain.dtype != torch.uint8 or plain.dim() != 2:
+        raise ValueError("plain must be a 2-D uint8 tensor")
+    rows, nblocks = plain.shape
+    if out is None:
+        out = _u8(rows * nblocks, plain.device)
+    _check(load().mx_swizzle_scales(_ptr(plain), rows, nblocks, _ptr(out), _stream(stream)), "mx_swizzle_scales")
     return out
 
 

@@ -461,6 +461,34 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
   return launch_status();
 }
 
+namespace {
+mx_status scale_layout(const void* src, int64_t rows, int64_t nblocks, void* dst, bool to_plain, void* stream) {
+  if (!src || !dst || rows <= 0 || nblocks <= 0 || rows % 128 || nblocks % 4) return MX_ERR_INVALID_ARG;
+  if (rows > (1ll << 40) / nblocks) return MX_ERR_INVALID_ARG;
+  const void* swz = to_plain ? src : dst;
+  const void* plain = to_plain ? dst : src;
+  if (!aligned(swz, 16) || !aligned(plain, 4)) return MX_ERR_INVALID_ARG;
+  const int sms = device_sms();
+  if (sms <= 0) return MX_ERR_CUDA;
+  const int64_t pieces = rows / 128 * (nblocks / 4) * 32;
+  int64_t grid = (pieces + 255) / 256;
+  if (grid > 8ll * sms) grid = 8ll * sms;
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  if (to_plain) scale_layout_kernel<true><<<static_cast<unsigned>(grid), 256, 0, as_stream(stream)>>>(s, d, rows, nblocks);
+  else scale_layout_kernel<false><<<static_cast<unsigned>(grid), 256, 0, as_stream(stream)>>>(s, d, rows, nblocks);
+  return launch_status();
+}
+}  // namespace
+
+mx_status mx_unswizzle_scales(const void* s_gemm, int64_t rows, int64_t nblocks, void* s_plain, void* stream) {
+  return scale_layout(s_gemm, rows, nblocks, s_plain, true, stream);
+}
+
+mx_status mx_swizzle_scales(const void* s_plain, int64_t rows, int64_t nblocks, void* s_gemm, void* stream) {
+  return scale_layout(s_plain, rows, nblocks, s_gemm, false, stream);
+}
+
 }  // extern "C"
 
 namespace {

@@ -408,6 +408,41 @@ __global__ void __launch_bounds__(128) mx_scales_from_blocks_kernel(const float*
   *reinterpret_cast<uint32_t*>(out + (rb * nkc + kc) * 512 + chunk_offset(i, 0)) = code * 0x01010101u;
 }
 
+// Byte permutation between the GEMM scale layout (512-byte chunks of 128 rows x 4 blocks, chunk
+// (rb, kc) at (rb * nblocks/4 + kc) * 512, in-chunk byte chunk_offset(i, j)) and a plain
+// [rows][nblocks] byte matrix.  The 16 bytes at in-chunk offset 16 * r hold rows r, r + 32,
+// r + 64, r + 96, four blocks each, so one thread moves one 16-byte piece as four 4-byte rows.
+// TO_PLAIN: src = GEMM layout, dst = plain; otherwise the inverse.
+template <bool TO_PLAIN>
+__global__ void __launch_bounds__(256) scale_layout_kernel(const uint8_t* __restrict__ src,
+                                                           uint8_t* __restrict__ dst, int64_t rows,
+                                                           int64_t nblocks) {
+  const int64_t kchunks = nblocks >> 2;
+  const int64_t pieces = (rows >> 7) * kchunks * 32;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < pieces;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t chunk = t >> 5;
+    const int r = static_cast<int>(t & 31);
+    const int64_t rb = chunk / kchunks, kc = chunk - rb * kchunks;
+    const int64_t swz = chunk * 512 + chunk_offset(r, 0);
+    const int64_t plain = ((rb << 7) + r) * nblocks + (kc << 2);
+    if constexpr (TO_PLAIN) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + swz);
+      *reinterpret_cast<uint32_t*>(dst + plain) = v.x;
+      *reinterpret_cast<uint32_t*>(dst + plain + 32 * nblocks) = v.y;
+      *reinterpret_cast<uint32_t*>(dst + plain + 64 * nblocks) = v.z;
+      *reinterpret_cast<uint32_t*>(dst + plain + 96 * nblocks) = v.w;
+    } else {
+      uint4 v;
+      v.x = *reinterpret_cast<const uint32_t*>(src + plain);
+      v.y = *reinterpret_cast<const uint32_t*>(src + plain + 32 * nblocks);
+      v.z = *reinterpret_cast<const uint32_t*>(src + plain + 64 * nblocks);
+      v.w = *reinterpret_cast<const uint32_t*>(src + plain + 96 * nblocks);
+      *reinterpret_cast<uint4*>(dst + swz) = v;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // DeepSeek 1x128: s = fl32(amax / 448) (1 if amax == 0), q = E4M3(fl32(x / s)); s stored
 // [K/128][rows].  CTA = 64 rows x one 128-column k-block; 4 lanes per row, 32 bf16 per lane (four

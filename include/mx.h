@@ -192,6 +192,20 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
                                      void* stream);
 
 /*
+ * mx_unswizzle_scales / mx_swizzle_scales -- byte permutations between the GEMM scale layout
+ * (the chunked layout described at the top of this header, as the quantizers write it and the
+ * GEMMs read it) and a plain row-major matrix s_plain[rows][nblocks], one byte per block:
+ * nblocks = K/32 for MX (E8M0) scales and K/16 for NVFP4 (E4M3) scales of a [rows][K] code
+ * matrix.  For inspecting scales, comparing them with another implementation, or bringing in
+ * scales computed elsewhere.  Both buffers are device memory of rows*nblocks bytes and must not
+ * overlap; the chunked one 16-byte aligned, the plain one 4-byte aligned.
+ * rows % 128 == 0, nblocks % 4 == 0, else MX_ERR_INVALID_ARG.  No arithmetic: bytes move as
+ * they are.
+ */
+mx_status mx_unswizzle_scales(const void* s_gemm, int64_t rows, int64_t nblocks, void* s_plain, void* stream);
+mx_status mx_swizzle_scales(const void* s_plain, int64_t rows, int64_t nblocks, void* s_gemm, void* stream);
+
+/*
  * mx_gemm_mxout -- MXFP8 GEMM whose epilogue quantizes its own results for the next product
  * (producer-side fusion of the MX quantization; [MX] sec 0.1 rule, [DS] sec 9 quantizes the
  * activations that feed the next FP8 product before they leave).

@@ -132,6 +132,20 @@ def test_scale_conversion_rejects_bad_arguments(lib):
     assert mx.mx_scale_bytes(256, 512, 128, 128, mx.SCALE_FP32_POW2) == 4 * 2 * 4
 
 
+def test_scale_layout_permutations_reject_bad_arguments(lib):
+    for f in (lib.mx_unswizzle_scales, lib.mx_swizzle_scales):
+        assert f(None, 128, 4, FAKE, None) == mx.MX_ERR_INVALID_ARG
+        assert f(FAKE, 128, 4, None, None) == mx.MX_ERR_INVALID_ARG
+        assert f(FAKE, 96, 4, FAKE, None) == mx.MX_ERR_INVALID_ARG       # rows not a multiple of 128
+        assert f(FAKE, 128, 6, FAKE, None) == mx.MX_ERR_INVALID_ARG      # blocks not a multiple of 4
+        assert f(FAKE, 128, 0, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    # the chunked side must be 16-byte aligned, the plain side 4-byte aligned
+    assert lib.mx_unswizzle_scales(FAKE + 4, 128, 4, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_unswizzle_scales(FAKE, 128, 4, FAKE + 2, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_swizzle_scales(FAKE + 2, 128, 4, FAKE, None) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_swizzle_scales(FAKE, 128, 4, FAKE + 4, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_dual_quantize_rejects_bad_arguments(lib):
     d = lib.mx_quantize_dual
     ptrs = [FAKE] * 8

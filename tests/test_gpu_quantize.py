@@ -12,7 +12,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
-from tests.layouts import chunked_to_plain
+from tests.layouts import chunked_to_plain, plain_to_chunked
 
 pytestmark = pytest.mark.gpu
 
@@ -228,3 +228,31 @@ def test_nvfp4_exhaustive_element_grid():
     out = np.zeros(rows * cols, np.uint16)
     out[: len(blk)] = blk
     check_nv(bits_to_bf16(out.reshape(rows, cols)))
+
+
+# ------------------------------------------------------------------ scale layout permutations
+@pytest.mark.parametrize("rows,nblocks", [(128, 4), (384, 12), (256, 512), (16384, 128)])
+def test_scale_layout_permutations_random_bytes(rows, nblocks):
+    # the library's byte permutation against the test-side one, and swizzle o unswizzle = identity
+    g = torch.Generator().manual_seed(rows * 7 + nblocks)
+    plain = torch.randint(0, 256, (rows, nblocks), dtype=torch.uint8, generator=g)
+    chunked = mx.mx_swizzle_scales(plain.cuda())
+    assert np.array_equal(chunked.cpu().numpy(), plain_to_chunked(plain.numpy()))
+    back = mx.mx_unswizzle_scales(chunked, rows, nblocks)
+    assert torch.equal(back.cpu(), plain)
+    assert mx.mx_check() == mx.MX_OK
+
+
+def test_unswizzled_scales_match_the_oracle():
+    # MX scales (K/32 blocks) and NVFP4 scales (K/16 blocks) of the quantizers, unswizzled on the
+    # device, equal the oracle's plain per-block scales
+    x = synthetic.with_sparse_outliers(256, 512, 4100)
+    _, osc = orc.mx_quantize_rowwise(x, orc.E4M3)
+    _, osT = orc.mx_quantize_colwise(x, orc.E4M3)
+    _, sr, _, sc = mx.mx_quantize(x.cuda(), elem=mx.E4M3, layout=mx.BOTH)
+    assert np.array_equal(mx.mx_unswizzle_scales(sr, 256, 512 // 32).cpu().numpy(), osc)
+    assert np.array_equal(mx.mx_unswizzle_scales(sc, 512, 256 // 32).cpu().numpy(), osT)
+    _, onv, _ = orc.nv_quantize(x)
+    _, snv, _ = mx.nvfp4_quantize(x.cuda())
+    assert np.array_equal(mx.mx_unswizzle_scales(snv, 256, 512 // 16).cpu().numpy(), onv)
+    assert mx.mx_check() == mx.MX_OK
