@@ -178,6 +178,20 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
                       max_clusters, st, ta, tb, tsa, tsb, tout, args);
 }
 
+// DeepSeek CTA-pair kernel, 256 x 256 output tiles.
+template <bool OUT_BF16>
+mx_status launch_ds_gemm2(const void* qa, const void* qb, const GemmArgs& args, cudaStream_t st) {
+  using Cfg = Ds2Cfg<OUT_BF16>;
+  static int max_clusters[64] = {};
+  CUtensorMap ta, tb, tout;
+  if (!make_tmap(&ta, qa, args.M, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
+  if (!make_tmap(&tb, qb, args.N, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
+  if (!make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)) return MX_ERR_CUDA;
+  const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
+  return launch_pairs(ds_gemm2_kernel<OUT_BF16>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters, st, ta, tb,
+                      tout, args);
+}
+
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
 // Quantizer grids are 2-D, x = row tiles (< 2^31), y = column tiles (at most 65535), so that no
 // thread divides 64-bit integers to find its tile.
@@ -608,6 +622,11 @@ mx_status fp8_blockwise_gemm(const void* qa, const float* sa, const void* qb, co
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   cudaStream_t st = as_stream(stream);
+  if (M % 256 == 0 && N % 256 == 0) {  // CTA pairs, 256 x 256 tiles
+    a.idesc = make_idesc_f8f6f4(0u, 0u, 256, 256);
+    if (out_dtype == MX_OUT_BF16) return launch_ds_gemm2<true>(qa, qb, a, st);
+    return launch_ds_gemm2<false>(qa, qb, a, st);
+  }
   a.idesc = make_idesc_f8f6f4(0u, 0u, 128, 128);
   if (out_dtype == MX_OUT_BF16) return launch_gemm<kDsF8, 128, true>(qa, qb, K, a, st);
   return launch_gemm<kDsF8, 128, false>(qa, qb, K, a, st);

@@ -463,4 +463,250 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
   if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------------------------
+// DeepSeek FP8 GEMM on the CTA pair ("Why FP8 training is stable" (magicnetworld.com), sec 6.3):
+// 256 x 256 output tiles, 128 rows per CTA.  Every 128-wide k-block is one TMA stage and four
+// kind::f8f6f4 MMAs (M = 256, N = 256: each SM multiplies 128 x 256 per instruction, so every
+// operand byte it reads from shared memory feeds twice the work of a 128 x 128 tile) into one of
+// two 256-column TMEM buffers, which fill all 512 columns.  The epilogue warps keep the tile's FP32 accumulators in registers (each warp
+// 32 rows x 128 columns, i.e. one 128-column weight block, so one scale pair per k-block) and
+// promote every k-block as acc += sA[kb][m] * sB[n/128][kb] * P: they read P from TMEM in
+// 16-column pieces, the next piece's load overlapping the current piece's paired FMAs, and hand
+// the buffer back right after the last piece landed, while the tensor core fills the other one.
+// (Measured: 32-column pieces with registers moved from the control warps to the epilogue by
+// setmaxnreg ran 12% slower at 4096 x 2048 x 7168.)
+// ---------------------------------------------------------------------------------------------
+template <bool OUT_BF16>
+struct Ds2Cfg {
+  static constexpr int BM = 256;
+  static constexpr int BN = 256;
+  static constexpr int ROWS = 128;     // A rows and B rows each CTA loads
+  static constexpr int KBYTES = 128;   // one k-block of E4M3 codes per stage
+  static constexpr int A_BYTES = ROWS * KBYTES;
+  static constexpr int B_BYTES = ROWS * KBYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_BYTES = 1024;
+  static constexpr int CHUNK_BYTES = OUT_BF16 ? 2048 : 4096;
+  static constexpr int STAGING = 8 * CHUNK_BYTES + 1024;
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING + BAR_BYTES;
+  static constexpr int NUM_MMA = KBYTES / 32;
+  static constexpr int NBUF = 2;
+  static constexpr int BUF_COLS = BN;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int NUM_EPI_WARPS = 8;
+  static constexpr int EPI_WARP = 2;  // warp 0: producer, warp 1: MMA issuer, 2-9: epilogue
+  static constexpr int THREADS = 32 * (EPI_WARP + NUM_EPI_WARPS);
+  static_assert(STAGES >= 2, "not enough shared memory");
+  static_assert(NBUF * BUF_COLS <= TMEM_COLS, "TMEM overflow");
+};
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
+    ds_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
+  using Cfg = Ds2Cfg<OUT_BF16>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + Cfg::STAGES * Cfg::A_BYTES;
+  uint8_t* sOut = sB + Cfg::STAGES * Cfg::B_BYTES;  // 1 KB aligned: stages are multiples of 1 KB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cfg::STAGING);
+  uint64_t* full_bar = bars;                       // [STAGES], used in the leader
+  uint64_t* empty_bar = bars + Cfg::STAGES;        // [STAGES], both CTAs
+  uint64_t* tfull_bar = bars + 2 * Cfg::STAGES;    // [NBUF], both CTAs
+  uint64_t* tempty_bar = tfull_bar + Cfg::NBUF;    // [NBUF], used in the leader
+  uint64_t* drain_bar = tempty_bar + Cfg::NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int num_mb = args.M / Cfg::BM;
+  const int num_nb = args.N / Cfg::BN;
+  const int num_tiles = num_mb * num_nb;
+  const int num_kt = args.K / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < Cfg::NBUF; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 2 * Cfg::NUM_EPI_WARPS);  // one arrival per epilogue warp of the pair
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+        int mb, nb;
+        tile_coords(tile, num_mb, num_nb, mb, nb);
+        const int a_row = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
+        const int b_row = nb * Cfg::BN + static_cast<int>(rank) * Cfg::ROWS;
+        for (int kt = 0; kt < num_kt; ++kt) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = map_to_rank(smem_u32(&full_bar[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * Cfg::STAGE_BYTES);
+          tma_load_2d_pair(sA + stage * Cfg::A_BYTES, &tmA, full_leader, kt * Cfg::KBYTES, a_row);
+          tma_load_2d_pair(sB + stage * Cfg::B_BYTES, &tmB, full_leader, kt * Cfg::KBYTES, b_row);
+          ++issued;
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // drain: the leader's stage barriers count both CTAs' bytes, so the leader waits for every
+      // copy either CTA issued; the final cluster barrier keeps the peer alive until then
+      if (leader) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+          if (issued > s) {
+            const long last = s + ((issued - 1 - s) / Cfg::STAGES) * Cfg::STAGES;
+            mbar_wait(&full_bar[s], static_cast<uint32_t>((last / Cfg::STAGES) & 1), abort_flag, kSiteDrain);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      constexpr uint32_t kOpHi = smem_desc_hi(1024, kSwizzle128B);
+      constexpr uint32_t kLbo = smem_desc_lo_lbo(16);
+      const uint32_t a_lo0 = (smem_u32(sA) >> 4) | kLbo, b_lo0 = (smem_u32(sB) >> 4) | kLbo;
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_it = 0;  // k-block partial products handed over so far
+      bool ok = true;
+      for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+        for (int kt = 0; kt < num_kt; ++kt) {
+          const uint32_t b = acc_it & 1;
+          if (!mbar_wait(&tempty_bar[b], ((acc_it >> 1) & 1) ^ 1, abort_flag, kSiteMmaTmemEmpty) ||
+              !mbar_wait(&full_bar[stage], phase, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + stage * (Cfg::A_BYTES >> 4);
+          const uint32_t b_lo = b_lo0 + stage * (Cfg::B_BYTES >> 4);
+          const uint32_t d_tmem = tmem_base + b * Cfg::BUF_COLS;
+#pragma unroll
+          for (int j = 0; j < Cfg::NUM_MMA; ++j)
+            umma_f8f6f4_pair(d_tmem, desc_from_words(a_lo + j * 2, kOpHi), desc_from_words(b_lo + j * 2, kOpHi),
+                             args.idesc, j > 0 ? 1u : 0u);
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          umma_commit_pair(&tfull_bar[b], 0x3);  // one k-block ready for promotion in both CTAs
+          ++acc_it;
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      umma_commit_pair(drain_bar, 0x1);
+      mbar_wait(drain_bar, 0, abort_flag, kSiteDrain);
+    }
+  } else {
+    // ------------------------------------------------------------------ promotion epilogue
+    const int q = warp & 3;                       // TMEM lane quarter
+    const int half = (warp - Cfg::EPI_WARP) >> 2;  // which 128-column weight block of the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tempty_leader0 = map_to_rank(smem_u32(&tempty_bar[0]), 0);
+    const int64_t kbs = num_kt;
+    uint8_t* buf = sOut + (warp - Cfg::EPI_WARP) * Cfg::CHUNK_BYTES;
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+      int mb, nb;
+      tile_coords(tile, num_mb, num_nb, mb, nb);
+      const int32_t row0 = mb * Cfg::BM + static_cast<int32_t>(rank) * Cfg::ROWS + q * 32;
+      const float* sa_row = args.dsa + row0 + lane;
+      const float* sb_blk = args.dsb + static_cast<int64_t>(2 * nb + half) * kbs;
+      float nsa = __ldg(sa_row), nsb = __ldg(sb_blk);
+      uint64_t acc[64];  // this thread's 128 FP32 accumulators as pairs
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0ull;
+      for (int kt = 0; kt < num_kt; ++kt) {
+        const float s = __fmul_rn(nsa, nsb);
+        if (kt + 1 < num_kt) {
+          nsa = __ldg(sa_row + static_cast<int64_t>(kt + 1) * args.M);
+          nsb = __ldg(sb_blk + kt + 1);
+        }
+        const uint32_t b = acc_it & 1;
+        ok = mbar_wait(&tfull_bar[b], (acc_it >> 1) & 1, abort_flag, kSiteEpiTmemFull);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + lane_addr + b * Cfg::BUF_COLS + half * 128;
+        const uint64_t s2 = pack_f32x2(s, s);
+        uint32_t r[2][16];
+        tmem_ld_32x32b_x16(taddr, r[0]);
+        tmem_ld_wait();
+        tmem_regs_ready16(r[0]);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c < 7) tmem_ld_32x32b_x16(taddr + (c + 1) * 16, r[(c + 1) & 1]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) fma2_scalar(acc[c * 8 + i], s2, r[c & 1][2 * i], r[c & 1][2 * i + 1]);
+          if (c < 7) {
+            tmem_ld_wait();
+            tmem_regs_ready16(r[(c + 1) & 1]);
+          }
+          if (c == 6) {
+            // every piece of P is in registers: hand the buffer back before the last FMAs
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8 * b);
+          }
+        }
+        ++acc_it;
+      }
+      if (!ok) break;
+      // the tile's 32 rows x 128 columns, as four 32 x 32 TMA stores through the staging buffer
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) unpack_f32x2(acc[c * 16 + i], v[2 * i], v[2 * i + 1]);
+        store_chunk_32x32<OUT_BF16>(&tmOut, buf, v, lane, nb * Cfg::BN + half * 128 + c * 32, row0);
+      }
+    }
+  }
+
+  if (warp >= Cfg::EPI_WARP && lane == 0) bulk_wait_all();
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+}
+
 }  // namespace mxgb
