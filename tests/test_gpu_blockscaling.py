@@ -13,6 +13,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
+from tests import quantized
 from tests.layouts import chunked_to_plain, plain_to_chunked
 from tests.test_gpu_gemm import assert_close
 
@@ -85,13 +86,13 @@ def test_scale_conversion_marks_non_powers_of_two():
 def block_scaled_through_mx(a, b, out_dtype):
     M, K = a.shape
     N = b.shape[0]
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), block=128, block_rows=1, sfmt=mx.SCALE_FP32_POW2, layout=mx.ROWWISE)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), block=128, block_rows=128, sfmt=mx.SCALE_FP32_POW2, layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.ds(a, 1, pow2=True)
+    qb, sb, oqb, osb = quantized.ds(b, 128, pow2=True)
     ea = mx.mx_scales_from_fp32_blocks(sa, M, K, 1)
     eb = mx.mx_scales_from_fp32_blocks(sb, N, K, 128)
     y = mx.mx_gemm(qa, ea, mx.E4M3, qb, eb, mx.E4M3, M, N, K, out_dtype=out_dtype)
     assert mx.mx_check() == mx.MX_OK
-    return y, qa, sa, qb, sb
+    return y, oqa, osa, oqb, osb
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 384, 256), (256, 256, 512), (512, 768, 1024)])
@@ -100,7 +101,7 @@ def test_block_scaled_product_through_mx_gemm(M, N, K, out_dtype):
     a = synthetic.normal(M, K, 1.0, 5420 + K)
     b = synthetic.normal(N, K, 0.02, 5421 + K)
     y, qa, sa, qb, sb = block_scaled_through_mx(a, b, out_dtype)
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb)
     assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="float8 blocks via mx")
 
 
@@ -110,7 +111,7 @@ def test_block_scaled_product_through_mx_gemm_full_size():
     N = b.shape[0]
     y, qa, sa, qb, sb = block_scaled_through_mx(a, b, mx.OUT_BF16)
     rows = np.array([0, 7, 128, 2049, 4095])
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy(), rows=rows)
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, ab, bf16=True, what="full size")
 
 
@@ -160,14 +161,13 @@ def test_2d32_weights_in_fprop_and_dgrad():
     x = synthetic.normal(M, K, 1.0, 5430)
     w = synthetic.normal(N, K, 0.02, 5431)
     g = synthetic.normal(M, N, 1e-3, 5432)
-    qx, sx, _, _ = mx.mx_quantize(x.cuda(), layout=mx.ROWWISE)
-    qw, sw, qwT, swT = mx.mx_quantize(w.cuda(), block=32, block_rows=32, layout=mx.BOTH)
-    qg, sg, _, _ = mx.mx_quantize(g.cuda(), elem=mx.E5M2, layout=mx.ROWWISE)
+    qx, sx, oqx, osx = quantized.mx_rowwise(x, orc.E4M3)
+    (qw, sw, qwT, swT), (oqw, osw, oqwT, oswT) = quantized.mx_both(w, orc.E4M3, block_rows=32)
+    qg, sg, oqg, osg = quantized.mx_rowwise(g, orc.E5M2)
     y = mx.mx_gemm(qx, sx, mx.E4M3, qw, sw, mx.E4M3, M, N, K, out_dtype=mx.OUT_F32)          # fprop
     dx = mx.mx_gemm(qg, sg, mx.E5M2, qwT, swT, mx.E4M3, M, K, N, out_dtype=mx.OUT_F32)      # dgrad
     assert mx.mx_check() == mx.MX_OK
-    for out, qa, sa, fa, qb, sb, m_, n_, k_ in ((y, qx, sx, orc.E4M3, qw, sw, M, N, K),
-                                                (dx, qg, sg, orc.E5M2, qwT, swT, M, K, N)):
-        ref, ab = orc.mx_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), m_, k_ // 32), fa,
-                              qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), n_, k_ // 32), orc.E4M3)
+    for out, ref_args in ((y, (oqx, osx, orc.E4M3, oqw, osw, orc.E4M3)),
+                          (dx, (oqg, osg, orc.E5M2, oqwT, oswT, orc.E4M3))):
+        ref, ab = orc.mx_gemm(*ref_args)
         assert_close(out.cpu().numpy(), ref, ab, what="2-D weights")

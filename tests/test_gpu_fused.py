@@ -1,15 +1,20 @@
 """GPU parity of the MXFP8 GEMM with its MX output quantization fused into the epilogue
-(mx_gemm_mxout): codes and scales equal the oracle's row-wise MX quantization of the same
-kernel's FP32 results (mx_gemm with FP32 output, checked against the double-precision oracle
-product), bit for bit -- the decision is taken in the kernel's precision, FP32.  Also: Inf
-results, E5M2 output, and the fused output used directly as the A operand of the next product.
+(mx_gemm_mxout).  The decision is taken in the kernel's precision, FP32, so the operands are
+built for exact FP32 sums: every A and B value is a signed power of two (E4M3 codes with a zero
+mantissa) and the scales are constant along K for each row and column, so within one output all
+products are multiples of one power of two and span at most 2^6 of it; with K <= 4096 every
+partial sum, in any order, is an integer below 2^18 in those units and exact in FP32.  The
+oracle's double-precision product is then exactly the FP32 value the kernel quantizes, and the
+expected codes and scales are the oracle's MX quantization of the oracle's product -- nothing on
+the reference side comes from the GPU.  Cases: E4M3 and E5M2 outputs, several tile counts, the
+full 8192 x 14336 x 4096 fprop shape on sampled rows, Inf results, and the fused output used
+directly as the A operand of the next product.
 """
 import numpy as np
 import pytest
 import torch
 
 import block_scaled_precision_mx_gb300 as mx
-from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
 from tests.layouts import chunked_to_plain, plain_to_chunked
 from tests.test_gpu_gemm import assert_close
@@ -31,37 +36,49 @@ def dev(a):
 
 
 def operands(M, N, K, seed):
+    """Exact-sum operands: E4M3 codes of 0 or +-2^e (e = -1 .. 2), E8M0 scales constant along K
+    (2^-4 .. 2^4 per row of A, 2^-2 .. 2^2 per row of B)."""
     rng = np.random.default_rng(seed)
-    sign = lambda shape: rng.integers(0, 2, shape, dtype=np.uint8) << 7
-    qa = rng.integers(0, 0x7E, (M, K), dtype=np.uint8) | sign((M, K))
-    qb = rng.integers(0, 0x7E, (N, K), dtype=np.uint8) | sign((N, K))
-    sa = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
-    sb = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+
+    def codes(shape):
+        e = rng.integers(6, 10, shape, dtype=np.uint8)           # biased exponent 6..9: 2^-1 .. 2^2
+        q = (e << 3) | (rng.integers(0, 2, shape, dtype=np.uint8) << 7)
+        q[rng.random(shape) < 0.1] = 0
+        return q
+    qa, qb = codes((M, K)), codes((N, K))
+    sa = np.repeat((127 + (np.arange(M) * 7) % 9 - 4).astype(np.uint8)[:, None], K // 32, axis=1)
+    sb = np.repeat((127 + np.arange(N) % 5 - 2).astype(np.uint8)[:, None], K // 32, axis=1)
     return qa, sa, qb, sb
 
 
 def check_fused(qa, sa, qb, sb, M, N, K, fmt, rows=None):
+    """Fused codes and scales against the oracle's MX quantization of the oracle's product (exact
+    in FP32 for the operands above, which the kernel's FP32 results must equal)."""
     args = (dev(qa), dev(plain_to_chunked(sa)), mx.E4M3, dev(qb), dev(plain_to_chunked(sb)), mx.E4M3)
     y32 = mx.mx_gemm(*args, M, N, K, out_dtype=mx.OUT_F32)
     q, s = mx.mx_gemm_mxout(*args, M, N, K, out_elem=MXFMT[fmt])
     assert mx.mx_check() == mx.MX_OK
-    y = y32.cpu().numpy()
-    r = np.arange(M) if rows is None else rows
-    oq, osc = orc.mx_quantize_rowwise_f32(y[r], fmt)
+    r = np.arange(M) if rows is None else np.asarray(rows)
+    ref, _ = orc.mx_gemm(qa, sa, orc.E4M3, qb, sb, orc.E4M3, rows=None if rows is None else r)
+    with np.errstate(over="ignore"):
+        ref32 = ref.astype(np.float32)
+    finite = np.isfinite(ref32)
+    assert np.array_equal(ref32[finite].astype(np.float64), ref[finite]), "operands do not give exact FP32 sums"
+    y = y32.cpu().numpy()[r]
+    assert np.array_equal(y[finite], ref32[finite]), "FP32 results differ from the exact product"
+    oq, osc = orc.mx_quantize_rowwise_f32(ref32, fmt)
     qn = q.cpu().numpy()[r]
     bad = np.argwhere(qn != oq)
     assert bad.size == 0, f"codes differ at {bad[:5].tolist()}"
     assert np.array_equal(chunked_to_plain(s.cpu().numpy(), M, N // 32)[r], osc)
-    return y, q, s
+    return q, s, oq, osc
 
 
 @pytest.mark.parametrize("fmt", [orc.E4M3, orc.E5M2])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 1024)])
 def test_fused_quantization_equals_quantized_fp32_results(fmt, M, N, K):
     qa, sa, qb, sb = operands(M, N, K, M + N + K + fmt)
-    y, _, _ = check_fused(qa, sa, qb, sb, M, N, K, fmt)
-    ref, ab = orc.mx_gemm(qa, sa, orc.E4M3, qb, sb, orc.E4M3)
-    assert_close(y, ref, ab, what="FP32 results before quantization")
+    check_fused(qa, sa, qb, sb, M, N, K, fmt)
 
 
 def test_fused_quantization_inf_results():
@@ -70,33 +87,26 @@ def test_fused_quantization_inf_results():
     qa[5, :] = 0x7E
     sa[5, :] = 254                      # 448 * 2^127 in every element of row 5 -> Inf products
     qb[:, :] = 0x7E
-    _, q, s = check_fused(qa, sa, qb, sb, M, N, K, orc.E4M3)
+    q, s, _, _ = check_fused(qa, sa, qb, sb, M, N, K, orc.E4M3)
     assert (chunked_to_plain(s.cpu().numpy(), M, N // 32)[5] == 0xFF).all()
 
 
 def test_fused_full_size_fprop():
-    x, w, _ = synthetic.mxfp8_linear()
-    qx, sx, _, _ = mx.mx_quantize(x.cuda(), layout=mx.ROWWISE)
-    qw, sw, _, _ = mx.mx_quantize(w.cuda(), layout=mx.ROWWISE)
+    # the fprop shape of the linear-layer workload, exact-sum operands, sampled rows
     M, N, K = 8192, 14336, 4096
-    y32 = mx.mx_gemm(qx, sx, mx.E4M3, qw, sw, mx.E4M3, M, N, K, out_dtype=mx.OUT_F32)
-    q, s = mx.mx_gemm_mxout(qx, sx, mx.E4M3, qw, sw, mx.E4M3, M, N, K)
-    assert mx.mx_check() == mx.MX_OK
-    rows = np.array([0, 1, 255, 256, 4097, 8191])
-    oq, osc = orc.mx_quantize_rowwise_f32(y32.cpu().numpy()[rows], orc.E4M3)
-    assert np.array_equal(q.cpu().numpy()[rows], oq)
-    assert np.array_equal(chunked_to_plain(s.cpu().numpy(), M, N // 32)[rows], osc)
+    qa, sa, qb, sb = operands(M, N, K, 31)
+    check_fused(qa, sa, qb, sb, M, N, K, orc.E4M3, rows=[0, 1, 255, 256, 4097, 8191])
 
 
 def test_fused_output_feeds_the_next_product():
     # Y = X W1^T quantized in the epilogue, then Z = Y W2^T reading Y's codes and scales as A
     M, N1, N2, K = 256, 512, 256, 256
     qa, sa, qb, sb = operands(M, N1, K, 21)
-    _, q, s = check_fused(qa, sa, qb, sb, M, N1, K, orc.E4M3)
+    q, s, oq, osc = check_fused(qa, sa, qb, sb, M, N1, K, orc.E4M3)
     rng = np.random.default_rng(22)
     q2 = rng.integers(0, 0x7E, (N2, N1), dtype=np.uint8)
     s2 = rng.integers(120, 134, (N2, N1 // 32), dtype=np.uint8)
     z = mx.mx_gemm(q, s, mx.E4M3, dev(q2), dev(plain_to_chunked(s2)), mx.E4M3, M, N2, N1, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    ref, ab = orc.mx_gemm(q.cpu().numpy(), chunked_to_plain(s.cpu().numpy(), M, N1 // 32), orc.E4M3, q2, s2, orc.E4M3)
+    ref, ab = orc.mx_gemm(oq, osc, orc.E4M3, q2, s2, orc.E4M3)   # the oracle's codes (equal, checked above)
     assert_close(z.cpu().numpy(), ref, ab, what="chained product")

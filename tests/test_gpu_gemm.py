@@ -15,6 +15,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
+from tests import quantized
 from tests.layouts import chunked_to_plain, plain_to_chunked
 
 pytestmark = pytest.mark.gpu
@@ -132,12 +133,10 @@ def test_mx_gemm_one_hot_operand_probe(M):
 @pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
 def test_mx_gemm_512_workload(out_dtype):
     a, b = synthetic.mxfp8_gemm_512()
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), layout=mx.ROWWISE)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.mx_rowwise(a, orc.E4M3)
+    qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E4M3)
     y = mx.mx_gemm(qa, sa, mx.E4M3, qb, sb, mx.E4M3, 512, 512, 512, out_dtype=out_dtype)
     assert mx.mx_check() == mx.MX_OK
-    oqa, osa = qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), 512, 16)
-    oqb, osb = qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), 512, 16)
     ref, ab = orc.mx_gemm(oqa, osa, orc.E4M3, oqb, osb, orc.E4M3)
     assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="512^3")
 
@@ -148,11 +147,10 @@ def test_mx_gemm_shapes(M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
     a = (torch.randn(M, K, generator=g) * 3).to(torch.bfloat16)
     b = torch.randn(N, K, generator=g).to(torch.bfloat16)
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), layout=mx.ROWWISE, elem=mx.E5M2)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.mx_rowwise(a, orc.E5M2)
+    qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E4M3)
     y = mx.mx_gemm(qa, sa, mx.E5M2, qb, sb, mx.E4M3, M, N, K, out_dtype=mx.OUT_F32)
-    ref, ab = orc.mx_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), M, K // 32), orc.E5M2,
-                          qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), N, K // 32), orc.E4M3)
+    ref, ab = orc.mx_gemm(oqa, osa, orc.E5M2, oqb, osb, orc.E4M3)
     assert_close(y.cpu().numpy(), ref, ab, what=f"{M}x{N}x{K}")
 
 
@@ -161,27 +159,22 @@ def test_mx_gemm_strided_output():
     g = torch.Generator().manual_seed(3)
     a = torch.randn(M, K, generator=g).to(torch.bfloat16)
     b = torch.randn(N, K, generator=g).to(torch.bfloat16)
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), layout=mx.ROWWISE)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.mx_rowwise(a, orc.E4M3)
+    qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E4M3)
     big = torch.full((M, N + 64), 7.0, dtype=torch.float32, device="cuda")
     st = mx.load().mx_gemm(qa.data_ptr(), sa.data_ptr(), 0, qb.data_ptr(), sb.data_ptr(), 0, M, N, K,
                            big.data_ptr(), mx.OUT_F32, N + 64, torch.cuda.current_stream().cuda_stream)
     assert st == mx.MX_OK and mx.mx_check() == mx.MX_OK
-    ref, ab = orc.mx_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), M, K // 32), 0,
-                          qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), N, K // 32), 0)
+    ref, ab = orc.mx_gemm(oqa, osa, 0, oqb, osb, 0)
     assert_close(big[:, :N].cpu().numpy(), ref, ab)
     assert (big[:, N:] == 7.0).all()
 
 
 @pytest.fixture(scope="module")
 def linear_layer():
+    # each entry: (device q_row, s_row, q_col, s_col), (oracle codes / plain scales, same order)
     x, w, g = synthetic.mxfp8_linear()
-    xd, wd, gd = x.cuda(), w.cuda(), g.cuda()
-    X = mx.mx_quantize(xd, elem=mx.E4M3, layout=mx.BOTH)
-    W = mx.mx_quantize(wd, elem=mx.E4M3, layout=mx.BOTH)
-    G = mx.mx_quantize(gd, elem=mx.E5M2, layout=mx.BOTH)
-    del xd, wd, gd
-    return X, W, G
+    return quantized.mx_both(x, orc.E4M3), quantized.mx_both(w, orc.E4M3), quantized.mx_both(g, orc.E5M2)
 
 
 SAMPLE_ROWS = [0, 1, 127, 128, 4095, 5000, 8191]
@@ -189,22 +182,21 @@ SAMPLE_ROWS = [0, 1, 127, 128, 4095, 5000, 8191]
 
 @pytest.mark.parametrize("which", ["fprop", "dgrad", "wgrad"])
 def test_mx_linear_layer_full_size(linear_layer, which):
-    X, W, G = linear_layer
+    (Xd, Xo), (Wd, Wo), (Gd, Go) = linear_layer
     M_, K_, N_ = 8192, 4096, 14336
     if which == "fprop":      # Y[M,N] = X W^T
-        A, sA, ea, B, sB, eb, M, N, K = X[0], X[1], 0, W[0], W[1], 0, M_, N_, K_
+        a, b, ea, eb, M, N, K = (0, 1), (0, 1), 0, 0, M_, N_, K_
+        (A, Ao), (B, Bo) = (Xd, Xo), (Wd, Wo)
     elif which == "dgrad":    # dX[M,K] = G W : A = G row-wise, B = W column-wise
-        A, sA, ea, B, sB, eb, M, N, K = G[0], G[1], 1, W[2], W[3], 0, M_, K_, N_
+        a, b, ea, eb, M, N, K = (0, 1), (2, 3), 1, 0, M_, K_, N_
+        (A, Ao), (B, Bo) = (Gd, Go), (Wd, Wo)
     else:                     # dW[N,K] = G^T X : A = G column-wise, B = X column-wise
-        A, sA, ea, B, sB, eb, M, N, K = G[2], G[3], 1, X[2], X[3], 0, N_, K_, M_
-    y = mx.mx_gemm(A, sA, ea, B, sB, eb, M, N, K, out_dtype=mx.OUT_BF16)
+        a, b, ea, eb, M, N, K = (2, 3), (2, 3), 1, 0, N_, K_, M_
+        (A, Ao), (B, Bo) = (Gd, Go), (Xd, Xo)
+    y = mx.mx_gemm(A[a[0]], A[a[1]], ea, B[b[0]], B[b[1]], eb, M, N, K, out_dtype=mx.OUT_BF16)
     assert mx.mx_check() == mx.MX_OK
     rows = np.array(sorted(set(r % M for r in SAMPLE_ROWS + [M - 1, M // 2 + 3])))
-    qa = A.cpu().numpy()
-    sa = chunked_to_plain(sA.cpu().numpy(), M, K // 32)
-    qb = B.cpu().numpy()
-    sb = chunked_to_plain(sB.cpu().numpy(), N, K // 32)
-    ref, ab = orc.mx_gemm(qa, sa, ea, qb, sb, eb, rows=rows)
+    ref, ab = orc.mx_gemm(Ao[a[0]], Ao[a[1]], ea, Bo[b[0]], Bo[b[1]], eb, rows=rows)
     got = y[torch.from_numpy(rows).cuda()].float().cpu().numpy()
     assert_close(got, ref, ab, bf16=True, what=which)
 
@@ -242,37 +234,37 @@ def test_nvfp4_scale_outside_sum_identity():
 def test_nvfp4_gemm_random(M, N, K):
     a = synthetic.with_sparse_outliers(M, K, 4000 + M)
     b = synthetic.with_sparse_outliers(N, K, 4001 + N)
-    qa, sa, ga = mx.nvfp4_quantize(a.cuda())
-    qb, sb, gb = mx.nvfp4_quantize(b.cuda())
+    qa, sa, ga, oqa, osa, oga = quantized.nv(a)
+    qb, sb, gb, oqb, osb, ogb = quantized.nv(b)
     y = mx.nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    ref, ab = orc.nv_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), M, K // 16), ga.item(),
-                          qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), N, K // 16), gb.item())
+    ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb)
     assert_close(y.cpu().numpy(), ref, ab, what="nvfp4")
 
 
 def test_nvfp4_gemm_full_size():
     a, b = synthetic.nvfp4_pair()
-    qa, sa, ga = mx.nvfp4_quantize(a.cuda())
-    qb, sb, gb = mx.nvfp4_quantize(b.cuda())
+    qa, sa, ga, oqa, osa, oga = quantized.nv(a)
+    qb, sb, gb, oqb, osb, ogb = quantized.nv(b)
     M = N = K = 8192
     y = mx.nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
     rows = np.array([0, 1, 129, 4096, 8191])
-    ref, ab = orc.nv_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), M, K // 16), ga.item(),
-                          qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), N, K // 16), gb.item(), rows=rows)
+    ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="nvfp4 8192^3")
 
 
 # ------------------------------------------------------------------ DeepSeek
 def ds_run(a, b, out_dtype=mx.OUT_F32):
+    """GPU quantize (checked against the oracle) + GPU GEMM; returns the GPU result and the
+    oracle's codes and scales for the reference product."""
     M, K = a.shape
     N = b.shape[0]
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), block=128, block_rows=1, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), block=128, block_rows=128, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.ds(a, 1)
+    qb, sb, oqb, osb = quantized.ds(b, 128)
     y = mx.fp8_blockwise_gemm(qa, sa, qb, sb, M, N, K, out_dtype=out_dtype)
     assert mx.mx_check() == mx.MX_OK
-    return y, qa, sa, qb, sb
+    return y, oqa, osa, oqb, osb
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 256, 1024)])
@@ -280,7 +272,7 @@ def test_deepseek_gemm_small(M, N, K):
     a = synthetic.normal(M, K, 1.0, 5000 + K)
     b = synthetic.normal(N, K, 0.02, 5001 + K)
     y, qa, sa, qb, sb = ds_run(a, b)
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb)
     assert_close(y.cpu().numpy(), ref, ab, what="deepseek")
 
 
@@ -291,7 +283,7 @@ def test_deepseek_gemm_more_shapes(M, N, K, out_dtype):
     a = synthetic.normal(M, K, 1.0, 5100 + K)
     b = synthetic.normal(N, K, 0.02, 5101 + K)
     y, qa, sa, qb, sb = ds_run(a, b, out_dtype=out_dtype)
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb)
     assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="deepseek shapes")
 
 
@@ -308,7 +300,7 @@ def test_deepseek_gemm_scale_per_block():
     a = (a.float() * ra[:, None] * ka[None, :]).to(torch.bfloat16)
     b = (b.float() * nb_[:, None] * kb[None, :]).to(torch.bfloat16)
     y, qa, sa, qb, sb = ds_run(a, b)
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb)
     assert_close(y.cpu().numpy(), ref, ab, what="deepseek scales")
 
 
@@ -319,7 +311,7 @@ def test_deepseek_gemm_more_tiles_than_sms():
     b = synthetic.normal(N, K, 0.05, 5301)
     y, qa, sa, qb, sb = ds_run(a, b)
     rows = np.array([0, 255, 256, 1031, 2048, 3333, 4095])
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy(), rows=rows)
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="deepseek tiles")
 
 
@@ -329,7 +321,7 @@ def test_deepseek_gemm_full_size():
     N = b.shape[0]
     y, qa, sa, qb, sb = ds_run(a, b, out_dtype=mx.OUT_BF16)
     rows = np.array([0, 5, 128, 2049, 4095])
-    ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy(), rows=rows)
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, ab, bf16=True, what="deepseek full")
 
 
@@ -341,6 +333,6 @@ def test_deepseek_error_does_not_grow_with_k():
         a = synthetic.normal(128, K, 1.0, 7000 + K)
         b = synthetic.normal(128, K, 1.0, 7001 + K)
         y, qa, sa, qb, sb = ds_run(a, b)
-        ref, ab = orc.ds_gemm(qa.cpu().numpy(), sa.cpu().numpy().T.copy(), qb.cpu().numpy(), sb.cpu().numpy())
+        ref, ab = orc.ds_gemm(qa, sa, qb, sb)
         worst.append(assert_close(y.cpu().numpy(), ref, ab, what=f"K={K}"))
     assert max(worst) <= REL

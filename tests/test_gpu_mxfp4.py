@@ -15,6 +15,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
+from tests import quantized
 from tests.layouts import chunked_to_plain, pack_fp4, plain_to_chunked, unpack_fp4
 from tests.test_gpu_quantize import exhaustive_matrix
 from tests.test_gpu_gemm import assert_close
@@ -132,12 +133,10 @@ def test_mxfp4_gemm_one_hot_scale_per_block_position(M, N):
 def test_mxfp4_quantize_then_gemm_full_size():
     a, b = synthetic.mxfp4_pair()
     M = N = K = 8192
-    qa, sa, _, _ = mx.mx_quantize(a.cuda(), elem=mx.E2M1, layout=mx.ROWWISE)
-    qb, sb, _, _ = mx.mx_quantize(b.cuda(), elem=mx.E2M1, layout=mx.ROWWISE)
+    qa, sa, oqa, osa = quantized.mx_rowwise(a, orc.E2M1)
+    qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E2M1)
     y = mx.mx_gemm(qa, sa, mx.E2M1, qb, sb, mx.E2M1, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
     rows = np.array([0, 1, 255, 256, 4097, 8191])
-    ref, ab = orc.mx_gemm(unpack_fp4(qa.cpu().numpy()), chunked_to_plain(sa.cpu().numpy(), M, K // 32), orc.E2M1,
-                          unpack_fp4(qb.cpu().numpy()), chunked_to_plain(sb.cpu().numpy(), N, K // 32), orc.E2M1,
-                          rows=rows)
+    ref, ab = orc.mx_gemm(oqa, osa, orc.E2M1, oqb, osb, orc.E2M1, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="mxfp4 8192^3")

@@ -12,6 +12,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 from block_scaled_precision_mx_gb300 import synthetic
 import oracle as orc
+from tests import quantized
 from tests.layouts import chunked_to_plain, pack_fp4, unpack_fp4
 from tests.test_gpu_gemm import assert_close
 
@@ -43,7 +44,7 @@ def check_ex(x, rht, sr, seed=0):
     bad = np.argwhere(qn != oq)
     assert bad.size == 0, f"codes differ at {bad[:5].tolist()}: gpu {qn[tuple(bad[0])]} oracle {oq[tuple(bad[0])]}"
     assert np.array_equal(chunked_to_plain(s.cpu().numpy(), rows, cols // 16), osc)
-    return q, s, g
+    return q, s, g, (pack_fp4(oq), osc, og)
 
 
 @pytest.mark.parametrize("rht,sr", [(True, False), (False, True), (True, True)])
@@ -84,12 +85,11 @@ def test_transformed_operands_multiply_through_the_fp4_gemm():
     M, N, K = 256, 512, 1024
     a = synthetic.with_sparse_outliers(M, K, 4300)
     b = synthetic.with_sparse_outliers(N, K, 4301)
-    qa, sa, ga = check_ex(a, True, False)
-    qb, sb, gb = check_ex(b, True, False)
+    qa, sa, ga, oa = check_ex(a, True, False)
+    qb, sb, gb, ob = check_ex(b, True, False)
     y = mx.nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    ref, ab = orc.nv_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), M, K // 16), ga.item(),
-                          qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), N, K // 16), gb.item())
+    ref, ab = orc.nv_gemm(*oa, *ob)
     assert_close(y.cpu().numpy(), ref, ab, what="transformed operands")
 
 
@@ -104,7 +104,7 @@ def check_2d(x):
     assert np.array_equal(chunked_to_plain(sr.cpu().numpy(), rows, cols // 16), np.repeat(os2, 16, axis=0))
     assert np.array_equal(qc.cpu().numpy(), pack_fp4(oq.T))
     assert np.array_equal(chunked_to_plain(sc.cpu().numpy(), cols, rows // 16), np.repeat(os2.T, 16, axis=0))
-    return qr, sr, qc, sc, g
+    return (qr, sr, qc, sc, g), (pack_fp4(oq), np.repeat(os2, 16, axis=0), pack_fp4(oq.T), np.repeat(os2.T, 16, axis=0), og)
 
 
 @pytest.mark.parametrize("shape", [(128, 128), (256, 384), (384, 256), (8192, 8192)])
@@ -129,13 +129,12 @@ def test_nvfp4_2d16_weights_in_both_products():
     x = synthetic.with_sparse_outliers(M, K, 4500)
     w = synthetic.with_sparse_outliers(N, K, 4501)
     gr = synthetic.with_sparse_outliers(M, N, 4502)
-    qx, sx, gx = mx.nvfp4_quantize(x.cuda())
-    qg, sg_, gg = mx.nvfp4_quantize(gr.cuda())
-    qw, sw, qwT, swT, gw = check_2d(w)
+    qx, sx, gx, oqx, osx, ogx = quantized.nv(x)
+    qg, sg_, gg, oqg, osg, ogg = quantized.nv(gr)
+    (qw, sw, qwT, swT, gw), (oqw, osw, oqwT, oswT, ogw) = check_2d(w)
     y = mx.nvfp4_gemm(qx, sx, gx, qw, sw, gw, M, N, K, out_dtype=mx.OUT_F32)
     dx = mx.nvfp4_gemm(qg, sg_, gg, qwT, swT, gw, M, K, N, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    for out, qa, sa, ga, qb, sb, m_, n_, k_ in ((y, qx, sx, gx, qw, sw, M, N, K), (dx, qg, sg_, gg, qwT, swT, M, K, N)):
-        ref, ab = orc.nv_gemm(qa.cpu().numpy(), chunked_to_plain(sa.cpu().numpy(), m_, k_ // 16), ga.item(),
-                              qb.cpu().numpy(), chunked_to_plain(sb.cpu().numpy(), n_, k_ // 16), gw.item())
+    for out, ref_args in ((y, (oqx, osx, ogx, oqw, osw, ogw)), (dx, (oqg, osg, ogg, oqwT, oswT, ogw))):
+        ref, ab = orc.nv_gemm(*ref_args)
         assert_close(out.cpu().numpy(), ref, ab, what="2-D weights")
