@@ -33,6 +33,7 @@ EXPORTS = (
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
     "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
+    "mx_selftest_wait_timeout",
 )
 
 
@@ -82,6 +83,7 @@ def load():
             "mx_gemm_mxout": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, vp, vp, i64, vp]),
             "mx_unswizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_swizzle_scales": (i32, [vp, i64, i64, vp, vp]),
+            "mx_selftest_wait_timeout": (i32, [i64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -182,6 +184,12 @@ def mx_scales_from_fp32_blocks(s: torch.Tensor, rows: int, cols: int, block_rows
     st = load().mx_scales_from_fp32_blocks(_ptr(s), rows, cols, block_rows, _ptr(out), _stream(stream))
     _check(st, "mx_scales_from_fp32_blocks")
     return out
+
+
+def mx_selftest_wait_timeout(budget_us: int = 10000, stream=None):
+    """Make one device-side bounded wait run out (include/mx.h, mx_selftest_wait_timeout); the
+    next mx_check() reports MX_ERR_TIMEOUT."""
+    _check(load().mx_selftest_wait_timeout(budget_us, _stream(stream)), "mx_selftest_wait_timeout")
 
 
 def mx_unswizzle_scales(s: torch.Tensor, rows: int, nblocks: int, out=None, stream=None):

@@ -476,6 +476,29 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
 }
 
 namespace {
+// One CTA waits, through the bounded wait every kernel of the library uses, on an mbarrier that
+// nothing arrives on: the wait runs out after budget_ns, sets the abort flag and its bit in the
+// device error word, and the kernel returns.
+__global__ void selftest_wait_kernel(unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, kSiteSelfTest, budget_ns);
+}
+}  // namespace
+
+mx_status mx_selftest_wait_timeout(int64_t budget_us, void* stream) {
+  if (budget_us < 1 || budget_us > 1000000) return MX_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<unsigned long long>(budget_us) * 1000ull);
+  return launch_status();
+}
+
+namespace {
 mx_status scale_layout(const void* src, int64_t rows, int64_t nblocks, void* dst, bool to_plain, void* stream) {
   if (!src || !dst || rows <= 0 || nblocks <= 0 || rows % 128 || nblocks % 4) return MX_ERR_INVALID_ARG;
   if (rows > (1ll << 40) / nblocks) return MX_ERR_INVALID_ARG;

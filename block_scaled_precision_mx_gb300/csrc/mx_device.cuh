@@ -28,6 +28,7 @@ enum WaitSite : unsigned int {
   kSiteEpiTmemFull = 1u << 3,
   kSiteDrain = 1u << 4,
   kSiteBadGroups = 1u << 5,  // not a wait: grouped GEMM offsets that break their contract
+  kSiteSelfTest = 1u << 6,   // the bounded-wait self-test (mx_selftest_wait_timeout)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -73,14 +74,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  `abort_flag` (shared) lets
 // one timed-out role release every other role of the CTA promptly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int site) {
+                                          unsigned int site, unsigned long long budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+    if (globaltimer_ns() - t0 > budget_ns) {
       *abort_flag = 1;
       atomicOr(&g_mx_error_word, site);
       return false;

@@ -192,6 +192,16 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
                                      void* stream);
 
 /*
+ * mx_selftest_wait_timeout -- exercises the failure path of the device-side waits.  Launches one
+ * CTA that waits on an mbarrier nothing ever arrives on, through the same bounded wait the GEMM
+ * kernels use, with a budget of budget_us microseconds (1 .. 1000000) instead of the kernels'
+ * 2 s.  The wait runs out, records its site in the device error word and the kernel returns; the
+ * next mx_check() on the stream reports MX_ERR_TIMEOUT (and clears the word).  Nothing faults
+ * and the context stays usable.  Returns MX_ERR_INVALID_ARG for a budget out of range.
+ */
+mx_status mx_selftest_wait_timeout(int64_t budget_us, void* stream);
+
+/*
  * mx_unswizzle_scales / mx_swizzle_scales -- byte permutations between the GEMM scale layout
  * (the chunked layout described at the top of this header, as the quantizers write it and the
  * GEMMs read it) and a plain row-major matrix s_plain[rows][nblocks], one byte per block:

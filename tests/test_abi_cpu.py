@@ -146,6 +146,11 @@ def test_scale_layout_permutations_reject_bad_arguments(lib):
     assert lib.mx_swizzle_scales(FAKE, 128, 4, FAKE + 4, None) == mx.MX_ERR_INVALID_ARG
 
 
+def test_wait_selftest_rejects_bad_budgets(lib):
+    for budget in (0, -5, 1000001):
+        assert lib.mx_selftest_wait_timeout(budget, None) == mx.MX_ERR_INVALID_ARG
+
+
 def test_dual_quantize_rejects_bad_arguments(lib):
     d = lib.mx_quantize_dual
     ptrs = [FAKE] * 8
