@@ -12,8 +12,9 @@ One step = one pass over every row of the hot path, each on its own seeded synth
 An extra group, not part of the default step, is measured with --only mx4:
   mx4  MXFP4 8192^3: quantize A and B to E2M1 with E8M0 scales per 32 (row-wise), FP4 GEMM
        with the block scales in the MMA (FP32 out)
-  fuse fprop 8192x4096x14336 with the MX (E4M3) quantization of Y fused into the GEMM epilogue,
-       against the unfused pair (bf16 fprop, then row-wise MX quantize of Y)
+  fuse fprop 8192x4096x14336 with the MX (E4M3) quantization of Y fused into the GEMM epilogue
+       (row-wise, then row- and column-wise), against the unfused pair (bf16 fprop, then
+       row-wise MX quantize of Y)
   moe  grouped MXFP8 GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
        in multiples of 128, one launch (bf16 out)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
@@ -229,8 +230,9 @@ class Workload:
             self.X10q = (u8(8192, 4096), u8(sb(8192, 4096)))
             self.W10q = (u8(14336, 4096), u8(sb(14336, 4096)))
             self.Y10q = (u8(8192, 14336), u8(sb(8192, 14336)))
+            self.Y10qT = (u8(14336, 8192), u8(sb(14336, 8192)))
             self.Y10 = bf(8192, 14336)
-            self.launches_per_step += 3
+            self.launches_per_step += 4
             self._outs += [self.Y10q[0]]
         if "moe" in groups:
             m9, n9 = sum(MOE_SIZES), len(MOE_SIZES) * 14336
@@ -311,6 +313,10 @@ class Workload:
             mark("fusedgemm")
             mx.mx_gemm_mxout(self.X10q[0], self.X10q[1], mx.E4M3, self.W10q[0], self.W10q[1], mx.E4M3, 8192, 14336,
                              4096, q_out=self.Y10q[0], s_out=self.Y10q[1])
+            mark("fusedboth")
+            mx.mx_gemm_mxout_ex(self.X10q[0], self.X10q[1], mx.E4M3, self.W10q[0], self.W10q[1], mx.E4M3, 8192,
+                                14336, 4096, layout=mx.BOTH, q_row=self.Y10q[0], s_row=self.Y10q[1],
+                                q_col=self.Y10qT[0], s_col=self.Y10qT[1])
             mark("unfused")
             mx.mx_gemm(self.X10q[0], self.X10q[1], mx.E4M3, self.W10q[0], self.W10q[1], mx.E4M3, 8192, 14336, 4096,
                        mx.OUT_BF16, out=self.Y10)
@@ -361,7 +367,7 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "fusedgemm", "unfused"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "fusedgemm", "fusedboth", "unfused"]
 
 
 def row_report(name, ms, peaks):
@@ -378,7 +384,7 @@ def row_report(name, ms, peaks):
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
     f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "unfused": F_LIN}[name]
+         "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN, "unfused": F_LIN}[name]
     tf = f / s / 1e12
     peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
@@ -637,7 +643,7 @@ def main():
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
     row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN}
+                 "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
@@ -646,7 +652,7 @@ def main():
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
-               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "mx_gemm_mxout": ["fusedgemm"],
+               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
                "mx_gemm_then_quantize": ["unfused"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
@@ -654,7 +660,7 @@ def main():
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "mx_gemm_mxout": 1,
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "mx_gemm_mxout": 2,
                 "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])

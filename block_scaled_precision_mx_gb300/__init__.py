@@ -33,7 +33,7 @@ EXPORTS = (
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
     "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
-    "mx_selftest_wait_timeout",
+    "mx_selftest_wait_timeout", "mx_gemm_mxout_ex",
 )
 
 
@@ -84,6 +84,8 @@ def load():
             "mx_unswizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_swizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_selftest_wait_timeout": (i32, [i64, vp]),
+            "mx_gemm_mxout_ex": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, vp, vp, i64, vp, vp, i64,
+                                       vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -333,6 +335,31 @@ def mx_gemm_mxout(qa, sa, ea, qb, sb, eb, M, N, K, out_elem=E4M3, q_out=None, s_
                               _ptr(s_out), q_out.stride(0), _stream(stream))
     _check(st, "mx_gemm_mxout")
     return q_out, s_out
+
+
+def mx_gemm_mxout_ex(qa, sa, ea, qb, sb, eb, M, N, K, out_elem=E4M3, layout=BOTH, q_row=None, s_row=None,
+                     q_col=None, s_col=None, stream=None):
+    """MXFP8 GEMM with row-wise and / or column-wise MX quantization of its results in the epilogue
+    (include/mx.h, mx_gemm_mxout_ex).  Returns (q_row [M][N], s_row, q_col [N][M], s_col); copies
+    not requested are None; scales are flat uint8 in the MX GEMM layout."""
+    dev = qa.device
+    row, col = bool(layout & ROWWISE), bool(layout & COLWISE)
+    if row and q_row is None:
+        q_row = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    if row and s_row is None:
+        s_row = _u8(M * N // 32, dev)
+    if col and q_col is None:
+        q_col = torch.empty(N, M, dtype=torch.uint8, device=dev)
+    if col and s_col is None:
+        s_col = _u8(M * N // 32, dev)
+    if not row:
+        q_row = s_row = None
+    if not col:
+        q_col = s_col = None
+    st = load().mx_gemm_mxout_ex(_ptr(qa), _ptr(sa), ea, _ptr(qb), _ptr(sb), eb, M, N, K, out_elem, layout,
+                                 _ptr(q_row), _ptr(s_row), N, _ptr(q_col), _ptr(s_col), M, _stream(stream))
+    _check(st, "mx_gemm_mxout_ex")
+    return q_row, s_row, q_col, s_col
 
 
 def mx_gemm_grouped(qa, sa, ea, qb, sb, eb, group_offsets, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):

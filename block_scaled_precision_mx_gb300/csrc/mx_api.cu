@@ -167,10 +167,12 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
   if (!make_tmap(&tb, qb, brows, kbytes, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tsa, args.sfa, (args.M / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
   if (!make_tmap(&tsb, args.sfb, (brows / 128) * kc * 4, 128, chunk_rows, false)) return MX_ERR_CUDA;
-  // (MX output: the epilogue stores codes itself; the map describes the code buffer as FP32
-  // words and is never used)
-  const bool ok_out = MXOUT >= 0 ? make_out_tmap(&tout, args.q_out, args.M, args.N / 4, args.ldc / 4, false)
-                                 : make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16);
+  // (MX output: the epilogue stores codes itself; the map describes a code buffer as FP32 words
+  // and is never used)
+  const bool ok_out =
+      MXOUT < 0 ? make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)
+      : args.q_out ? make_out_tmap(&tout, args.q_out, args.M, args.N / 4, args.ldc / 4, false)
+                   : make_out_tmap(&tout, args.q_col, args.N, args.M / 4, args.ldq_col / 4, false);
   if (!ok_out) return MX_ERR_CUDA;
   // grouped: the tile count is known on the device only; every co-resident cluster runs
   const int tiles = GROUPED ? 0x7FFFFFFF : (args.M / Cfg::BM) * (args.N / Cfg::BN);
@@ -398,15 +400,21 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
   return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
 }
 
-mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
-                        int64_t M, int64_t N, int64_t K, mx_elem out_elem, void* q_out, void* s_out, int64_t ldq,
-                        void* stream) {
-  if (!qa || !sa || !qb || !sb || !q_out || !s_out) return MX_ERR_INVALID_ARG;
+mx_status mx_gemm_mxout_ex(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                           int64_t M, int64_t N, int64_t K, mx_elem out_elem, mx_layout layout, void* q_row,
+                           void* s_row, int64_t ldq_row, void* q_col, void* s_col, int64_t ldq_col, void* stream) {
+  if (layout != MX_ROWWISE && layout != MX_COLWISE && layout != MX_BOTH) return MX_ERR_INVALID_ARG;
+  const bool row = layout & MX_ROWWISE, col = layout & MX_COLWISE;
+  if (!qa || !sa || !qb || !sb) return MX_ERR_INVALID_ARG;
+  if (row && (!q_row || !s_row)) return MX_ERR_INVALID_ARG;
+  if (col && (!q_col || !s_col)) return MX_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 128) return MX_ERR_INVALID_ARG;
-  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30) || ldq < N || ldq % 16) return MX_ERR_INVALID_ARG;
-  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(q_out, 16) ||
-      !aligned(s_out, 16))
-    return MX_ERR_INVALID_ARG;
+  if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return MX_ERR_INVALID_ARG;
+  if (row && (ldq_row < N || ldq_row % 16)) return MX_ERR_INVALID_ARG;
+  if (col && (ldq_col < M || ldq_col % 16)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16)) return MX_ERR_INVALID_ARG;
+  if (row && (!aligned(q_row, 16) || !aligned(s_row, 16))) return MX_ERR_INVALID_ARG;
+  if (col && (!aligned(q_col, 16) || !aligned(s_col, 16))) return MX_ERR_INVALID_ARG;
   if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
     if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
     return MX_ERR_INVALID_ARG;
@@ -415,16 +423,33 @@ mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* 
   GemmArgs a{};
   a.sfa = static_cast<const uint8_t*>(sa);
   a.sfb = static_cast<const uint8_t*>(sb);
-  a.q_out = static_cast<uint8_t*>(q_out);
-  a.s_out = static_cast<uint8_t*>(s_out);
-  a.ldc = ldq;
+  a.q_out = row ? static_cast<uint8_t*>(q_row) : nullptr;
+  a.s_out = row ? static_cast<uint8_t*>(s_row) : nullptr;
+  a.ldc = row ? ldq_row : N;
+  a.q_col = col ? static_cast<uint8_t*>(q_col) : nullptr;
+  a.s_col = col ? static_cast<uint8_t*>(s_col) : nullptr;
+  a.ldq_col = ldq_col;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
   a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
   cudaStream_t st = as_stream(stream);
-  if (out_elem == MX_E4M3) return launch_gemm2<kMxf8, false, false, 0>(qa, qb, K, a, st);
-  return launch_gemm2<kMxf8, false, false, 1>(qa, qb, K, a, st);
+  const bool e4 = out_elem == MX_E4M3;
+  if (layout == MX_ROWWISE)
+    return e4 ? launch_gemm2<kMxf8, false, false, mxout_code(0, 1)>(qa, qb, K, a, st)
+              : launch_gemm2<kMxf8, false, false, mxout_code(1, 1)>(qa, qb, K, a, st);
+  if (layout == MX_COLWISE)
+    return e4 ? launch_gemm2<kMxf8, false, false, mxout_code(0, 2)>(qa, qb, K, a, st)
+              : launch_gemm2<kMxf8, false, false, mxout_code(1, 2)>(qa, qb, K, a, st);
+  return e4 ? launch_gemm2<kMxf8, false, false, mxout_code(0, 3)>(qa, qb, K, a, st)
+            : launch_gemm2<kMxf8, false, false, mxout_code(1, 3)>(qa, qb, K, a, st);
+}
+
+mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                        int64_t M, int64_t N, int64_t K, mx_elem out_elem, void* q_out, void* s_out, int64_t ldq,
+                        void* stream) {
+  return mx_gemm_mxout_ex(qa, sa, ea, qb, sb, eb, M, N, K, out_elem, MX_ROWWISE, q_out, s_out, ldq, nullptr, nullptr,
+                          0, stream);
 }
 
 mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,

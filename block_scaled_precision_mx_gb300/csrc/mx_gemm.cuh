@@ -98,8 +98,11 @@ struct GemmArgs {
   uint32_t idesc;
   const int64_t* group_off;  // grouped GEMM: device int64[groups + 1] row offsets of the groups
   int groups;
-  uint8_t* q_out;  // MX output: codes [M][ldc bytes] and E8M0 scales in the MX GEMM layout
-  uint8_t* s_out;
+  uint8_t* q_out;  // MX output, row-wise: codes [M][ldc bytes] and E8M0 scales in the MX GEMM
+  uint8_t* s_out;  // layout (either may be skipped by passing null codes)
+  uint8_t* q_col;  // MX output, column-wise: codes [N][ldq_col bytes] (the transpose of the
+  uint8_t* s_col;  // result, blocks of 32 rows) and E8M0 scales in the MX GEMM layout of [N][M]
+  int64_t ldq_col;
 };
 
 constexpr int kMaxGroups = 1024;

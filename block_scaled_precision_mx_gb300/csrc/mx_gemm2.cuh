@@ -111,11 +111,14 @@ struct Gemm2Cfg {
 // off[g] .. off[g+1] of A by the g-th [N][K] block of B into the same rows of C; tiles are
 // numbered group by group (the per-group tile counts' prefix sums sit in shared memory) and a
 // CTA whose 128 rows lie past its group's last row computes but stores nothing.
-// MXOUT >= 0 (0 = E4M3, 1 = E5M2): the epilogue quantizes its FP32 results itself, row-wise in
-// 1x32 blocks with the MX rule, and writes codes and E8M0 scales (in the layout the next MX
-// product reads as its A operand) instead of bf16 / FP32 values -- the producer-side fusion of
-// the next layer's quantization ("Why FP8 training is stable" (magicnetworld.com), sec 9: the
-// activations feeding the next FP8 product are quantized before they leave).
+// MXOUT >= 0: the epilogue quantizes its FP32 results itself with the MX rule and writes codes
+// and E8M0 scales instead of bf16 / FP32 values -- the producer-side fusion of the next layer's
+// quantization ("Why FP8 training is stable" (magicnetworld.com), sec 9: the activations feeding
+// the next FP8 product are quantized before they leave).  MXOUT = format + 2 * copies: format 0
+// E4M3, 1 E5M2; copies 1 row-wise (1x32 blocks, the next product's A operand), 2 column-wise
+// (32x1 blocks, stored transposed: the operand of a product reducing over M), 3 both.  Each copy
+// is compiled in only where it is written.
+constexpr int mxout_code(int fmt, int copies) { return fmt + 2 * copies; }
 template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THREADS, 1)
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -404,44 +407,88 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
       const int32_t y0 = static_cast<int32_t>(a_row0 + rank * Cfg::ROWS + q * 32);
       if (!store) continue;
       if constexpr (MXOUT >= 0) {
-        // this thread's row holds 4 whole 1x32 blocks (its 128 columns): amax, E8M0 byte
-        // max(exp(amax) - emax, 0) (0xFF with codes 0x7F for Inf / NaN), codes of x * 2^-k
-        constexpr int kEmax = (MXOUT == 0) ? 8 : 15;
+        constexpr int kFmt = MXOUT & 1;
+        constexpr bool kRowCopy = (MXOUT >> 1) & 1;
+        constexpr bool kColCopy = (MXOUT >> 2) & 1;
+        constexpr int kEmax = (kFmt == 0) ? 8 : 15;
         const int64_t row = y0 + lane;
         const int64_t col0 = static_cast<int64_t>(nb) * Cfg::BN + half * HALF;
-        uint32_t sbytes = 0;
+        // both copies are produced chunk by chunk (32 columns at a time), so each chunk's
+        // accumulator registers are dead once its codes are out
+        uint32_t sbytes = 0;                     // row-wise scale bytes of the 4 chunks
+        const int64_t sc_base = (col0 >> 7) * (args.M >> 7) * 512 + (static_cast<int64_t>(y0) >> 7) * 512;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          uint32_t m = 0;
+          if constexpr (kRowCopy) {
+            // row-wise: this thread's row holds the chunk's whole 1x32 block: amax, E8M0 byte
+            // max(exp(amax) - emax, 0) (0xFF with codes 0x7F for Inf / NaN), codes of x * 2^-k
+            uint32_t m = 0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) m = max(m, r[c][i] & 0x7FFFFFFFu);
-          uint32_t sb, w[8];
-          if (m >= 0x7F800000u) {
-            sb = 0xFF;
+            for (int i = 0; i < 32; ++i) m = max(m, r[c][i] & 0x7FFFFFFFu);
+            uint32_t sb, w[8];
+            if (m >= 0x7F800000u) {
+              sb = 0xFF;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = 0x7F7F7F7Fu;
-          } else {
-            const int e = static_cast<int>(m >> 23);
-            sb = e > kEmax ? static_cast<uint32_t>(e - kEmax) : 0u;
-            const float inv = __uint_as_float((254u - sb) << 23);  // 2^-(sb - 127), always normal
+              for (int k = 0; k < 8; ++k) w[k] = 0x7F7F7F7Fu;
+            } else {
+              const int e = static_cast<int>(m >> 23);
+              sb = e > kEmax ? static_cast<uint32_t>(e - kEmax) : 0u;
+              const float inv = __uint_as_float((254u - sb) << 23);  // 2^-(sb - 127), always normal
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float f0 = __fmul_rn(__uint_as_float(r[c][4 * k]), inv);
-              const float f1 = __fmul_rn(__uint_as_float(r[c][4 * k + 1]), inv);
-              const float f2 = __fmul_rn(__uint_as_float(r[c][4 * k + 2]), inv);
-              const float f3 = __fmul_rn(__uint_as_float(r[c][4 * k + 3]), inv);
-              w[k] = (MXOUT == 0) ? (cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16))
-                                  : (cvt_e5m2x2(f0, f1) | (cvt_e5m2x2(f2, f3) << 16));
+              for (int k = 0; k < 8; ++k) {
+                const float f0 = __fmul_rn(__uint_as_float(r[c][4 * k]), inv);
+                const float f1 = __fmul_rn(__uint_as_float(r[c][4 * k + 1]), inv);
+                const float f2 = __fmul_rn(__uint_as_float(r[c][4 * k + 2]), inv);
+                const float f3 = __fmul_rn(__uint_as_float(r[c][4 * k + 3]), inv);
+                w[k] = (kFmt == 0) ? (cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16))
+                                   : (cvt_e5m2x2(f0, f1) | (cvt_e5m2x2(f2, f3) << 16));
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(args.q_out + row * args.ldc + col0 + c * 32);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            sbytes |= sb << (8 * c);
+          }
+          if constexpr (kColCopy) {
+            // column-wise: the warp's 32 lanes are the 32 rows of one 32x1 block of every column,
+            // so a block's amax is one warp reduction; lane l writes row l's code of each column
+            // into the transposed copy (32 consecutive bytes per column) and lane i the scale byte
+            // of column i, at (column, 32-row block y0 / 32) of the [N][M/32] scales
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint32_t m0 = __reduce_max_sync(0xFFFFFFFFu, r[c][i] & 0x7FFFFFFFu);
+              const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, r[c][i + 1] & 0x7FFFFFFFu);
+              uint32_t sb0 = 0xFF, sb1 = 0xFF;
+              float f0 = 0.0f, f1 = 0.0f;
+              if (m0 < 0x7F800000u) {
+                const int e = static_cast<int>(m0 >> 23);
+                sb0 = e > kEmax ? static_cast<uint32_t>(e - kEmax) : 0u;
+                f0 = __fmul_rn(__uint_as_float(r[c][i]), __uint_as_float((254u - sb0) << 23));
+              }
+              if (m1 < 0x7F800000u) {
+                const int e = static_cast<int>(m1 >> 23);
+                sb1 = e > kEmax ? static_cast<uint32_t>(e - kEmax) : 0u;
+                f1 = __fmul_rn(__uint_as_float(r[c][i + 1]), __uint_as_float((254u - sb1) << 23));
+              }
+              uint32_t w = (kFmt == 0) ? cvt_e4m3x2(f0, f1) : cvt_e5m2x2(f0, f1);
+              if (sb0 == 0xFF) w = (w & 0xFF00u) | 0x7Fu;
+              if (sb1 == 0xFF) w = (w & 0x00FFu) | 0x7F00u;
+              const int64_t col = col0 + c * 32 + i;
+              args.q_col[col * args.ldq_col + y0 + lane] = static_cast<uint8_t>(w & 0xFFu);
+              args.q_col[(col + 1) * args.ldq_col + y0 + lane] = static_cast<uint8_t>(w >> 8);
+              if (lane == i) {
+                const int ci = static_cast<int>(col & 127);
+                args.s_col[sc_base + chunk_offset_mx(ci) + q] = static_cast<uint8_t>(sb0);
+                args.s_col[sc_base + chunk_offset_mx(ci + 1) + q] = static_cast<uint8_t>(sb1);
+              }
             }
           }
-          uint4* dst = reinterpret_cast<uint4*>(args.q_out + row * args.ldc + col0 + c * 32);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          sbytes |= sb << (8 * c);
         }
-        // chunk (row / 128, 128-column block of this half) of the [M][N/32] scales
-        *reinterpret_cast<uint32_t*>(args.s_out + ((row >> 7) * (args.N >> 7) + (col0 >> 7)) * 512 +
-                                     chunk_offset_mx(static_cast<int>(row & 127))) = sbytes;
+        if constexpr (kRowCopy) {
+          // chunk (row / 128, 128-column block of this half) of the [M][N/32] scales
+          *reinterpret_cast<uint32_t*>(args.s_out + ((row >> 7) * (args.N >> 7) + (col0 >> 7)) * 512 +
+                                       chunk_offset_mx(static_cast<int>(row & 127))) = sbytes;
+        }
       } else {
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {

@@ -232,6 +232,21 @@ mx_status mx_gemm_mxout(const void* qa, const void* sa, mx_elem ea, const void* 
                         void* stream);
 
 /*
+ * mx_gemm_mxout_ex -- mx_gemm_mxout with the copies a training step needs ([MX] sec 1.2: a
+ * transpose needs its own blocks, scales and codes): layout MX_ROWWISE writes the row-wise copy
+ * exactly as mx_gemm_mxout (q_row[M][ldq_row], s_row in the MX GEMM layout of [M][N]);
+ * MX_COLWISE writes the column-wise copy -- 32x1 blocks down each column of the result, stored
+ * transposed like mx_quantize's column-wise output: q_col[N][ldq_col] codes (ldq_col >= M,
+ * ldq_col % 16 == 0) and s_col: M*N/32 bytes in the MX GEMM layout of [N][M], i.e. the operand of
+ * a following product that reduces over M; MX_BOTH writes both from the same FP32 results.  Same
+ * scale and code rule as mx_gemm_mxout per block.  Pointers of a copy not requested may be NULL.
+ * M % 256 == 0, N % 256 == 0, K % 128 == 0.
+ */
+mx_status mx_gemm_mxout_ex(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
+                           int64_t M, int64_t N, int64_t K, mx_elem out_elem, mx_layout layout, void* q_row,
+                           void* s_row, int64_t ldq_row, void* q_col, void* s_col, int64_t ldq_col, void* stream);
+
+/*
  * mx_gemm_grouped -- MXFP8 expert GEMMs of a mixture-of-experts layer in one launch.  [MX]
  * sec 1.2 (grouped GEMM is its own entry point besides the single GEMMs).
  *

@@ -151,6 +151,24 @@ def test_wait_selftest_rejects_bad_budgets(lib):
         assert lib.mx_selftest_wait_timeout(budget, None) == mx.MX_ERR_INVALID_ARG
 
 
+def test_fused_output_ex_rejects_bad_arguments(lib):
+    f = lib.mx_gemm_mxout_ex
+    base = [FAKE, FAKE, mx.E4M3, FAKE, FAKE, mx.E4M3, 256, 256, 256, mx.E4M3]
+    ok_row = [FAKE, FAKE, 256]
+    ok_col = [FAKE, FAKE, 256]
+    assert f(*base, 0, *ok_row, *ok_col, None) == mx.MX_ERR_INVALID_ARG             # no layout
+    assert f(*base, mx.COLWISE, *ok_row, None, FAKE, 256, None) == mx.MX_ERR_INVALID_ARG
+    assert f(*base, mx.ROWWISE, None, FAKE, 256, *ok_col, None) == mx.MX_ERR_INVALID_ARG
+    assert f(*base, mx.COLWISE, None, None, 0, FAKE, FAKE, 128, None) == mx.MX_ERR_INVALID_ARG   # ldq_col < M
+    assert f(*base, mx.COLWISE, None, None, 0, FAKE + 8, FAKE, 256, None) == mx.MX_ERR_INVALID_ARG
+    b2 = list(base)
+    b2[6] = 128                                                                         # M not a multiple of 256
+    assert f(*b2, mx.BOTH, *ok_row, *ok_col, None) == mx.MX_ERR_INVALID_ARG
+    b3 = list(base)
+    b3[9] = mx.E2M1
+    assert f(*b3, mx.BOTH, *ok_row, *ok_col, None) == mx.MX_ERR_UNSUPPORTED
+
+
 def test_dual_quantize_rejects_bad_arguments(lib):
     d = lib.mx_quantize_dual
     ptrs = [FAKE] * 8

@@ -74,6 +74,74 @@ def check_fused(qa, sa, qb, sb, M, N, K, fmt, rows=None):
     return q, s, oq, osc
 
 
+def check_fused_ex(qa, sa, qb, sb, M, N, K, fmt, layout, cols=None):
+    """mx_gemm_mxout_ex: the row-wise copy as check_fused; the column-wise copy (32x1 blocks,
+    stored transposed) against the oracle's MX quantization of the transposed oracle product, on
+    all output columns or the sampled ones (each column needs all M rows of the product)."""
+    args = (dev(qa), dev(plain_to_chunked(sa)), mx.E4M3, dev(qb), dev(plain_to_chunked(sb)), mx.E4M3)
+    q, s, qT, sT = mx.mx_gemm_mxout_ex(*args, M, N, K, out_elem=MXFMT[fmt], layout=layout)
+    assert mx.mx_check() == mx.MX_OK
+    c = np.arange(N) if cols is None else np.asarray(cols)
+    ref, _ = orc.mx_gemm(qa, sa, orc.E4M3, qb[c], sb[c], orc.E4M3)      # [M][len(c)]
+    with np.errstate(over="ignore"):
+        ref32 = ref.astype(np.float32)
+    finite = np.isfinite(ref32)
+    assert np.array_equal(ref32[finite].astype(np.float64), ref[finite]), "operands do not give exact FP32 sums"
+    if layout & mx.ROWWISE and cols is None:
+        oq, osc = orc.mx_quantize_rowwise_f32(ref32, fmt)
+        assert np.array_equal(q.cpu().numpy(), oq), "row codes"
+        assert np.array_equal(chunked_to_plain(s.cpu().numpy(), M, N // 32), osc), "row scales"
+    if layout & mx.COLWISE:
+        oqT, osT = orc.mx_quantize_rowwise_f32(np.ascontiguousarray(ref32.T), fmt)   # [len(c)][M]
+        qTn = qT.cpu().numpy()[c]
+        bad = np.argwhere(qTn != oqT)
+        assert bad.size == 0, f"column codes differ at {bad[:5].tolist()}"
+        assert np.array_equal(chunked_to_plain(sT.cpu().numpy(), N, M // 32)[c], osT), "column scales"
+    return q, s, qT, sT
+
+
+@pytest.mark.parametrize("fmt", [orc.E4M3, orc.E5M2])
+@pytest.mark.parametrize("layout", [mx.COLWISE, mx.BOTH])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 1024), (768, 512, 128)])
+def test_fused_column_wise_copy(fmt, layout, M, N, K):
+    qa, sa, qb, sb = operands(M, N, K, 7 * M + N + K + fmt)
+    check_fused_ex(qa, sa, qb, sb, M, N, K, fmt, layout)
+
+
+def test_fused_column_wise_copy_inf_results():
+    M, N, K = 256, 256, 128
+    qa, sa, qb, sb = operands(M, N, K, 19)
+    qa[5, :] = 0x7E
+    sa[5, :] = 254                      # every result of row 5 is Inf -> every 32x1 block holding row 5
+    qb[:, :] = 0x7E
+    _, _, _, sT = check_fused_ex(qa, sa, qb, sb, M, N, K, orc.E4M3, mx.BOTH)
+    assert (chunked_to_plain(sT.cpu().numpy(), N, M // 32)[:, 0] == 0xFF).all()
+
+
+def test_fused_column_wise_full_size_fprop():
+    # the fprop shape of the linear-layer workload, exact-sum operands, sampled output columns
+    M, N, K = 8192, 14336, 4096
+    qa, sa, qb, sb = operands(M, N, K, 41)
+    check_fused_ex(qa, sa, qb, sb, M, N, K, orc.E4M3, mx.BOTH, cols=[0, 1, 127, 128, 7000, 14335])
+
+
+def test_fused_column_wise_copy_feeds_a_reduction_over_m():
+    # Y = X W^T with its column-wise copy quantized in the epilogue; Y^T's codes then serve as the
+    # A operand of a product reducing over M (the wgrad pattern)
+    M, N, K, P = 256, 512, 256, 256
+    qa, sa, qb, sb = operands(M, N, K, 23)
+    _, _, qT, sT = check_fused_ex(qa, sa, qb, sb, M, N, K, orc.E4M3, mx.COLWISE)
+    rng = np.random.default_rng(24)
+    q2 = rng.integers(0, 0x7E, (P, M), dtype=np.uint8)
+    s2 = rng.integers(120, 134, (P, M // 32), dtype=np.uint8)
+    z = mx.mx_gemm(qT, sT, mx.E4M3, dev(q2), dev(plain_to_chunked(s2)), mx.E4M3, N, P, M, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    ref, _ = orc.mx_gemm(qa, sa, orc.E4M3, qb, sb, orc.E4M3)
+    oqT, osT = orc.mx_quantize_rowwise_f32(np.ascontiguousarray(ref.astype(np.float32).T), orc.E4M3)
+    zr, ab = orc.mx_gemm(oqT, osT, orc.E4M3, q2, s2, orc.E4M3)
+    assert_close(z.cpu().numpy(), zr, ab, what="product of the column-wise copy")
+
+
 @pytest.mark.parametrize("fmt", [orc.E4M3, orc.E5M2])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 1024)])
 def test_fused_quantization_equals_quantized_fp32_results(fmt, M, N, K):
