@@ -33,7 +33,7 @@ EXPORTS = (
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
     "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
-    "mx_selftest_wait_timeout", "mx_gemm_mxout_ex",
+    "mx_selftest_wait_timeout", "mx_gemm_mxout_ex", "nvfp4_gemm_grouped",
 )
 
 
@@ -84,6 +84,7 @@ def load():
             "mx_unswizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_swizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_selftest_wait_timeout": (i32, [i64, vp]),
+            "nvfp4_gemm_grouped": (i32, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
             "mx_gemm_mxout_ex": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, vp, vp, i64, vp, vp, i64,
                                        vp]),
         }
@@ -335,6 +336,19 @@ def mx_gemm_mxout(qa, sa, ea, qb, sb, eb, M, N, K, out_elem=E4M3, q_out=None, s_
                               _ptr(s_out), q_out.stride(0), _stream(stream))
     _check(st, "mx_gemm_mxout")
     return q_out, s_out
+
+
+def nvfp4_gemm_grouped(qa, sa, ga, qb, sb, gb, group_offsets, M, N, K, out_dtype=OUT_F32, out=None, stream=None):
+    """NVFP4 grouped GEMM (include/mx.h, nvfp4_gemm_grouped): rows off[g] .. off[g+1] of A times the
+    g-th [N][K] block of B, scaled by ga * gb[g].  ga: float CUDA tensor [1]; gb: [G]."""
+    if group_offsets.dtype != torch.int64:
+        raise ValueError("group_offsets must be int64")
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().nvfp4_gemm_grouped(_ptr(qa), _ptr(sa), _ptr(ga), _ptr(qb), _ptr(sb), _ptr(gb), _ptr(group_offsets),
+                                   group_offsets.numel() - 1, M, N, K, out.data_ptr(), out_dtype, ldc,
+                                   _stream(stream))
+    _check(st, "nvfp4_gemm_grouped")
+    return out
 
 
 def mx_gemm_mxout_ex(qa, sa, ea, qb, sb, eb, M, N, K, out_elem=E4M3, layout=BOTH, q_row=None, s_row=None,

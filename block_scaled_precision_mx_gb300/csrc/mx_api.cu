@@ -157,7 +157,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
 template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st,
                        int64_t b_rows = 0) {
-  using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>;
+  using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUPED>;
   static int max_clusters[64] = {};
   const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte scale chunks per 128 rows
   const int chunk_rows = Cfg::SF_CHUNK / 128;
@@ -457,13 +457,14 @@ mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void
                           mx_out out_dtype, int64_t ldc, void* stream) {
   if (!qa || !sa || !qb || !sb || !out || !group_offsets) return MX_ERR_INVALID_ARG;
   if (groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
-  if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
+  const bool fp4 = ea == MX_E2M1 && eb == MX_E2M1;   // MXFP4 experts
+  if (!gemm_shape_ok(M, N, K, fp4 ? 256 : 128, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
   if (groups * N > (1ll << 30)) return MX_ERR_INVALID_ARG;
   if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16) ||
       !aligned(group_offsets, 8))
     return MX_ERR_INVALID_ARG;
-  if ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2)) {
-    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;
+  if (!fp4 && ((ea != MX_E4M3 && ea != MX_E5M2) || (eb != MX_E4M3 && eb != MX_E5M2))) {
+    if (ea == MX_E2M1 || eb == MX_E2M1) return MX_ERR_UNSUPPORTED;   // FP4 x FP8 mixes
     return MX_ERR_INVALID_ARG;
   }
   GemmArgs a{};
@@ -476,10 +477,43 @@ mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void
   a.K = static_cast<int>(K);
   a.group_off = group_offsets;
   a.groups = static_cast<int>(groups);
-  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
   cudaStream_t st = as_stream(stream);
+  if (fp4) {
+    a.idesc = make_idesc_block_scaled(1u, 1u, 256, 256, 1);
+    if (out_dtype == MX_OUT_BF16) return launch_gemm2<kMxf4, true, true>(qa, qb, K / 2, a, st, groups * N);
+    return launch_gemm2<kMxf4, false, true>(qa, qb, K / 2, a, st, groups * N);
+  }
+  a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 256, 256, 1);
   if (out_dtype == MX_OUT_BF16) return launch_gemm2<kMxf8, true, true>(qa, qb, K, a, st, groups * N);
   return launch_gemm2<kMxf8, false, true>(qa, qb, K, a, st, groups * N);
+}
+
+mx_status nvfp4_gemm_grouped(const void* qa, const void* sa, const float* ga, const void* qb, const void* sb,
+                             const float* gb, const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N,
+                             int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !ga || !qb || !sb || !gb || !out || !group_offsets) return MX_ERR_INVALID_ARG;
+  if (groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 256, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
+  if (groups * N > (1ll << 30)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 16) || !aligned(sb, 16) || !aligned(out, 16) ||
+      !aligned(ga, 4) || !aligned(gb, 4) || !aligned(group_offsets, 8))
+    return MX_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.sfa = static_cast<const uint8_t*>(sa);
+  a.sfb = static_cast<const uint8_t*>(sb);
+  a.ga = ga;
+  a.gb = gb;
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.group_off = group_offsets;
+  a.groups = static_cast<int>(groups);
+  a.idesc = make_idesc_block_scaled(1u, 1u, 256, 256, 0);
+  cudaStream_t st = as_stream(stream);
+  if (out_dtype == MX_OUT_BF16) return launch_gemm2<kNvf4, true, true>(qa, qb, K / 2, a, st, groups * N);
+  return launch_gemm2<kNvf4, false, true>(qa, qb, K / 2, a, st, groups * N);
 }
 
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols) {

@@ -64,7 +64,7 @@ __device__ __forceinline__ int chunk_offset_mx(int i) { return (i & 31) * 16 + (
 
 // NARROW_OUT: bf16 (or MX codes) out, whose 32 x 32 staging chunk is 2 KB instead of FP32's 4 KB;
 // the freed shared memory holds one more pipeline stage for MXFP8 (6 instead of 5: +3-5%).
-template <int KIND, bool NARROW_OUT = false>
+template <int KIND, bool NARROW_OUT = false, bool GROUPED_ = false>
 struct Gemm2Cfg {
   static constexpr int BM = 256;       // rows per pair tile (128 per CTA)
   static constexpr int BN = 256;       // columns per pair tile
@@ -82,7 +82,10 @@ struct Gemm2Cfg {
   // 128-byte swizzle
   static constexpr int CHUNK_BYTES = NARROW_OUT ? 2048 : 4096;
   static constexpr int STAGING = 8 * CHUNK_BYTES + 1024;
-  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING) / STAGE_BYTES;
+  // static shared memory of the kernel (the grouped kernels' table of group start tiles) comes
+  // out of the same per-CTA limit
+  static constexpr int STATIC_SMEM = GROUPED_ ? (kMaxGroups + 1) * 4 + 64 : 64;
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING - STATIC_SMEM) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING + BAR_BYTES;
   static constexpr int NUM_MMA = KBYTES / 32;
@@ -108,7 +111,8 @@ struct Gemm2Cfg {
 // is 4 such rows), so that the peer CTA's scale loads can complete on the leader's barrier too.
 // GROUPED (MoE expert GEMMs in one launch; "MXFP8 on SM120: software support"
 // (xuesongtap.github.io), sec 1.2: grouped GEMM is its own entry point): group g multiplies rows
-// off[g] .. off[g+1] of A by the g-th [N][K] block of B into the same rows of C; tiles are
+// off[g] .. off[g+1] of A by the g-th [N][K] block of B into the same rows of C (NVFP4: times
+// s_gA * s_gB[g], each expert's weights having their own global scale); tiles are
 // numbered group by group (the per-group tile counts' prefix sums sit in shared memory) and a
 // CTA whose 128 rows lie past its group's last row computes but stores nothing.
 // MXOUT >= 0: the epilogue quantizes its FP32 results itself with the MX rule and writes codes
@@ -120,11 +124,11 @@ struct Gemm2Cfg {
 // is compiled in only where it is written.
 constexpr int mxout_code(int fmt, int copies) { return fmt + 2 * copies; }
 template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
-__global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THREADS, 1)
+__global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUPED>::THREADS, 1)
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
-  using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>;
+  using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUPED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -201,8 +205,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
   // tile -> (first A row, first B row, rows of A that belong to it, output column block)
-  auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb) {
+  auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb, int& grp) {
     int mb;
+    grp = 0;
     if (GROUPED) {
       int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
       while (lo < hi) {
@@ -216,6 +221,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
       b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * Cfg::BN;
       const int64_t left = rows_g - static_cast<int64_t>(mb) * Cfg::BM;
       rows_valid = left < Cfg::BM ? static_cast<int>(left) : Cfg::BM;
+      grp = lo;
     } else {
       tile_coords(tile, num_mb, num_nb, mb, nb);
       a_row0 = static_cast<int64_t>(mb) * Cfg::BM;
@@ -234,8 +240,8 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
         int64_t a_row0, b_row0;
-        int rows_valid, nb;
-        decode(tile, a_row0, b_row0, rows_valid, nb);
+        int rows_valid, nb, grp;
+        decode(tile, a_row0, b_row0, rows_valid, nb, grp);
         const int a_row = static_cast<int>(a_row0) + static_cast<int>(rank) * Cfg::ROWS;
         const int b_row = static_cast<int>(b_row0) + static_cast<int>(rank) * Cfg::ROWS;
         for (int kt = 0; kt < num_kt; ++kt) {
@@ -382,12 +388,14 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0)>::THRE
     constexpr int HALF = Cfg::BN / 2;
     constexpr int NCH = HALF / 32;
     float gscale = 1.0f;
-    if (KIND == kNvf4) gscale = __fmul_rn(*args.ga, *args.gb);
+    if (KIND == kNvf4 && !GROUPED) gscale = __fmul_rn(*args.ga, *args.gb);
     uint32_t acc_it = 0;
     for (int tile = cluster; tile < num_tiles; tile += nclusters) {
       int64_t a_row0, b_row0;
-      int rows_valid, nb;
-      decode(tile, a_row0, b_row0, rows_valid, nb);
+      int rows_valid, nb, grp;
+      decode(tile, a_row0, b_row0, rows_valid, nb, grp);
+      // grouped NVFP4: every expert's B carries its own global scale
+      if (KIND == kNvf4 && GROUPED) gscale = __fmul_rn(*args.ga, __ldg(args.gb + grp));
       const bool store = static_cast<int>(rank) * Cfg::ROWS < rows_valid;  // this CTA's rows exist
       bool ok = mbar_wait(tfull_bar, acc_it & 1, abort_flag, kSiteEpiTmemFull);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;

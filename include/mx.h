@@ -259,11 +259,24 @@ mx_status mx_gemm_mxout_ex(const void* qa, const void* sa, mx_elem ea, const voi
  * expert sizes can come from device-side routing without a host round trip); they must satisfy
  * off[0] = 0, off[G] = M, off[g] <= off[g+1] and off[g] % 128 == 0 (an empty group is allowed).
  * Offsets that break this make the call do nothing and mx_check return MX_ERR_INVALID_ARG.
- * M % 128 == 0, N % 256 == 0, K % 128 == 0, element formats as mx_gemm (MXFP8 only).
+ * M % 128 == 0, N % 256 == 0, K % 128 == 0, element formats as mx_gemm: MXFP8 (E4M3 / E5M2) or
+ * MXFP4 (both MX_E2M1, codes packed as mx_quantize writes them, K % 256 == 0).
  */
 mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void* qb, const void* sb, mx_elem eb,
                           const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N, int64_t K, void* out,
                           mx_out out_dtype, int64_t ldc, void* stream);
+
+/*
+ * nvfp4_gemm_grouped -- NVFP4 expert GEMMs in one launch: group g computes, for its rows
+ * off[g] <= m < off[g+1],  C[m][n] = s_gA * s_gB[g] * sum_b sA[m][b] sB[gN + n][b] sum_{i<16} qA qB
+ * ([NV] sec 7.3-7.4; each expert's weights are quantized as their own tensor, so each has its own
+ * global scale).  qa[M][K/2] packed E2M1 with sa in the NVFP4 GEMM layout of [M][K] and one global
+ * scale ga (device float); qb[G*N][K/2] with sb the layout of [G*N][K] and gb: device float[G].
+ * group_offsets as mx_gemm_grouped.  M % 128 == 0, N % 256 == 0, K % 256 == 0.
+ */
+mx_status nvfp4_gemm_grouped(const void* qa, const void* sa, const float* ga, const void* qb, const void* sb,
+                             const float* gb, const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N,
+                             int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream);
 
 /* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);

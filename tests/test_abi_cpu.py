@@ -169,6 +169,26 @@ def test_fused_output_ex_rejects_bad_arguments(lib):
     assert f(*b3, mx.BOTH, *ok_row, *ok_col, None) == mx.MX_ERR_UNSUPPORTED
 
 
+def test_nvfp4_grouped_rejects_bad_arguments(lib):
+    f = lib.nvfp4_gemm_grouped
+    ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_F32, 256, None]
+    bad = list(ok); bad[2] = None                     # no global scale of A
+    assert f(*bad) == mx.MX_ERR_INVALID_ARG
+    bad = list(ok); bad[7] = 0                        # no groups
+    assert f(*bad) == mx.MX_ERR_INVALID_ARG
+    bad = list(ok); bad[10] = 128                     # K not a multiple of 256
+    assert f(*bad) == mx.MX_ERR_INVALID_ARG
+    bad = list(ok); bad[9] = 128                      # N not a multiple of 256
+    assert f(*bad) == mx.MX_ERR_INVALID_ARG
+    bad = list(ok); bad[6] = FAKE + 4                 # offsets not 8-byte aligned
+    assert f(*bad) == mx.MX_ERR_INVALID_ARG
+    g = lib.mx_gemm_grouped
+    assert g(FAKE, FAKE, mx.E2M1, FAKE, FAKE, mx.E4M3, FAKE, 1, 256, 256, 256, FAKE, mx.OUT_F32, 256,
+             None) == mx.MX_ERR_UNSUPPORTED              # FP4 x FP8 experts
+    assert g(FAKE, FAKE, mx.E2M1, FAKE, FAKE, mx.E2M1, FAKE, 1, 256, 256, 128, FAKE, mx.OUT_F32, 256,
+             None) == mx.MX_ERR_INVALID_ARG              # MXFP4 needs K % 256
+
+
 def test_dual_quantize_rejects_bad_arguments(lib):
     d = lib.mx_quantize_dual
     ptrs = [FAKE] * 8

@@ -11,7 +11,7 @@ import torch
 
 import block_scaled_precision_mx_gb300 as mx
 import oracle as orc
-from tests.layouts import chunked_to_plain, plain_to_chunked
+from tests.layouts import chunked_to_plain, pack_fp4, plain_to_chunked
 from tests.test_gpu_gemm import assert_close
 
 pytestmark = pytest.mark.gpu
@@ -92,3 +92,71 @@ def test_grouped_rejects_broken_offsets_on_the_device(off):
     assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
     assert bool((out == 7.0).all())
     assert mx.mx_check() == mx.MX_OK               # the error word was cleared
+
+
+# ------------------------------------------------------------------ FP4 experts
+def fp4_grouped_operands(M, G, N, K, seed, nv):
+    rng = np.random.default_rng(seed)
+    ca = rng.integers(0, 16, (M, K), dtype=np.uint8)          # E2M1 codes (all 16 are finite)
+    cb = rng.integers(0, 16, (G * N, K), dtype=np.uint8)
+    if nv:   # UE4M3 block scales per 16, positive and finite
+        sa = rng.integers(0x28, 0x48, (M, K // 16), dtype=np.uint8)
+        sb = rng.integers(0x28, 0x48, (G * N, K // 16), dtype=np.uint8)
+    else:    # E8M0 per 32
+        sa = rng.integers(118, 136, (M, K // 32), dtype=np.uint8)
+        sb = rng.integers(118, 136, (G * N, K // 32), dtype=np.uint8)
+    return ca, sa, cb, sb
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_grouped_mxfp4(out_dtype):
+    sizes, N, K = [256, 128, 0, 384], 512, 512
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    ca, sa, cb, sb = fp4_grouped_operands(M, G, N, K, 31, nv=False)
+    y = mx.mx_gemm_grouped(dev(pack_fp4(ca)), dev(plain_to_chunked(sa)), mx.E2M1, dev(pack_fp4(cb)),
+                           dev(plain_to_chunked(sb)), mx.E2M1, dev(off), M, N, K, out_dtype=out_dtype)
+    assert mx.mx_check() == mx.MX_OK
+    yn = y.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        ref, ab = orc.mx_gemm(ca[lo:hi], sa[lo:hi], orc.E2M1, cb[g * N:(g + 1) * N], sb[g * N:(g + 1) * N], orc.E2M1)
+        assert_close(yn[lo:hi], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"mxfp4 group {g}")
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_grouped_nvfp4_per_expert_global_scales(out_dtype):
+    sizes, N, K = [128, 384, 0, 256, 128], 256, 512
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    ca, sa, cb, sb = fp4_grouped_operands(M, G, N, K, 32, nv=True)
+    ga = np.float32(0.75)
+    gb = np.array([0.5, 1.25, 3.0, 0.125, 2.0], np.float32)
+    qa, qb = pack_fp4(ca), pack_fp4(cb)
+    y = mx.nvfp4_gemm_grouped(dev(qa), dev(plain_to_chunked(sa)), torch.tensor([ga], device="cuda"), dev(qb),
+                              dev(plain_to_chunked(sb)), torch.from_numpy(gb).cuda(), dev(off), M, N, K,
+                              out_dtype=out_dtype)
+    assert mx.mx_check() == mx.MX_OK
+    yn = y.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        ref, ab = orc.nv_gemm(qa[lo:hi], sa[lo:hi], float(ga), qb[g * N:(g + 1) * N], sb[g * N:(g + 1) * N], float(gb[g]))
+        assert_close(yn[lo:hi], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"nvfp4 group {g}")
+
+
+def test_grouped_nvfp4_single_group_equals_plain_gemm():
+    M, N, K = 512, 768, 1024
+    ca, sa, cb, sb = fp4_grouped_operands(M, 1, N, K, 33, nv=True)
+    ga = torch.tensor([0.5], device="cuda")
+    gb = torch.tensor([1.5], device="cuda")
+    args = (dev(pack_fp4(ca)), dev(plain_to_chunked(sa)), ga, dev(pack_fp4(cb)), dev(plain_to_chunked(sb)), gb)
+    y1 = mx.nvfp4_gemm(*args, M, N, K, out_dtype=mx.OUT_F32)
+    y2 = mx.nvfp4_gemm_grouped(*args, dev(np.array([0, M], np.int64)), M, N, K, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    assert torch.equal(y1, y2)
