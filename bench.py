@@ -15,8 +15,8 @@ An extra group, not part of the default step, is measured with --only mx4:
   fuse fprop 8192x4096x14336 with the MX (E4M3) quantization of Y fused into the GEMM epilogue
        (row-wise, then row- and column-wise), against the unfused pair (bf16 fprop, then
        row-wise MX quantize of Y)
-  moe  grouped MXFP8 GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
-       in multiples of 128, one launch (bf16 out)
+  moe  grouped GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
+       in multiples of 128, one launch (bf16 out), MXFP8 and NVFP4 (one global scale per expert)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
        stochastic rounding (random bytes read from HBM), both, and 16x16 2-D blocks written in
        both orientations
@@ -241,7 +241,12 @@ class Workload:
             self.off9 = torch.tensor([0] + list(__import__("itertools").accumulate(MOE_SIZES)), dtype=torch.int64,
                                      device=dev)
             self.Y9 = bf(m9, 14336)
-            self.launches_per_step += 1
+            # NVFP4 experts: the tokens as one tensor (one global scale), each expert's weights as
+            # their own tensor (one global scale each)
+            self.A9n = (u8(m9, 2048), u8(sb(m9, 4096, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
+            self.B9n = (u8(n9, 2048), u8(sb(n9, 4096, 16, 1, mx.SCALE_UE4M3)), f32(len(MOE_SIZES)),
+                        u8(16 * len(MOE_SIZES)))
+            self.launches_per_step += 2
             self._outs += [self.Y9]
         if "nvt" in groups:
             g8 = torch.Generator(device="cpu").manual_seed(8100)
@@ -326,9 +331,19 @@ class Workload:
                 mx.mx_quantize(d["A9"], layout=mx.ROWWISE, q_row=self.A9q[0], s_row=self.A9q[1])
                 mx.mx_quantize(d["B9"], layout=mx.ROWWISE, q_row=self.B9q[0], s_row=self.B9q[1])
                 self._moe_quantized = True
+                a, b = self.A9n, self.B9n
+                mx.nvfp4_quantize(d["A9"], q_packed=a[0], s_ue4m3=a[1], gscale=a[2], workspace=a[3])
+                per_expert = b[1].numel() // len(MOE_SIZES)        # scale bytes of 14336 rows
+                for e in range(len(MOE_SIZES)):
+                    mx.nvfp4_quantize(d["B9"][e * 14336:(e + 1) * 14336], q_packed=b[0][e * 14336:(e + 1) * 14336],
+                                      s_ue4m3=b[1][e * per_expert:(e + 1) * per_expert], gscale=b[2][e:e + 1],
+                                      workspace=b[3][16 * e:16 * (e + 1)])
             mark("moegemm")
             mx.mx_gemm_grouped(self.A9q[0], self.A9q[1], mx.E4M3, self.B9q[0], self.B9q[1], mx.E4M3, self.off9,
                                sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
+            mark("moe4gemm")
+            mx.nvfp4_gemm_grouped(self.A9n[0], self.A9n[1], self.A9n[2], self.B9n[0], self.B9n[1], self.B9n[2],
+                                  self.off9, sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
         if "nvt" in g:
             q = self.A8q
             mark("nvq_rht")
@@ -367,7 +382,7 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "fusedgemm", "fusedboth", "unfused"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "moe4gemm", "fusedgemm", "fusedboth", "unfused"]
 
 
 def row_report(name, ms, peaks):
@@ -384,9 +399,10 @@ def row_report(name, ms, peaks):
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
     f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN, "unfused": F_LIN}[name]
+         "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN,
+         "unfused": F_LIN}[name]
     tf = f / s / 1e12
-    peak = fp4_peak if name in ("nvgemm", "mx4gemm") else fp8_peak
+    peak = fp4_peak if name in ("nvgemm", "mx4gemm", "moe4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
             "flops": int(f)}
 
@@ -643,7 +659,7 @@ def main():
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
     row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS, "moegemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN}
+                 "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
@@ -652,7 +668,7 @@ def main():
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
-               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
+               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "nvfp4_gemm_grouped": ["moe4gemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
                "mx_gemm_then_quantize": ["unfused"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
@@ -660,7 +676,7 @@ def main():
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "mx_gemm_mxout": 2,
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "nvfp4_gemm_grouped": 1, "mx_gemm_mxout": 2,
                 "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
