@@ -323,8 +323,10 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
       else ds_quantize_1x128_kernel<false><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
     } else {
       if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-      if (pow2) ds_quantize_128x128_kernel<true><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
-      else ds_quantize_128x128_kernel<false><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
+      CUtensorMap tmx;  // x as bytes [rows][2 cols], boxes of 128 bytes x 128 rows
+      if (!make_tmap(&tmx, x, rows, cols * 2, 128, false)) return MX_ERR_CUDA;
+      if (pow2) ds_quantize_128x128_kernel<true><<<grid, 256, 0, st>>>(tmx, rows, cols, qo, so);
+      else ds_quantize_128x128_kernel<false><<<grid, 256, 0, st>>>(tmx, rows, cols, qo, so);
     }
     return launch_status();
   }

@@ -29,6 +29,7 @@ enum WaitSite : unsigned int {
   kSiteDrain = 1u << 4,
   kSiteBadGroups = 1u << 5,  // not a wait: grouped GEMM offsets that break their contract
   kSiteSelfTest = 1u << 6,   // the bounded-wait self-test (mx_selftest_wait_timeout)
+  kSiteQuantLoad = 1u << 7,  // a quantizer's wait for its staged input tile
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -87,6 +88,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       return false;
     }
   }
+}
+
+// Bounded wait that ignores the abort flag: used after an abort, so that copies still in flight
+// land before the CTA's shared memory is released.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long budget_ns) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > budget_ns) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------ TMA / bulk copies

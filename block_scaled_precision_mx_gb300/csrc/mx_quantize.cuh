@@ -493,24 +493,43 @@ __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* 
   if (l4 == 0) s[kb * rows + r] = sc;
 }
 
-// DeepSeek 128x128 weight blocks: one CTA per block; 256 threads x 64 elements in registers.
+// DeepSeek 128x128 weight blocks: one CTA per block.  The block (32 KB) arrives in shared memory
+// as two TMA boxes of 128 rows x 64 columns; the threads read it twice from there (block maximum,
+// then codes), so few registers stay live and six CTAs share an SM: a 2048 x 7168 weight (896
+// blocks) runs as one wave on 152 SMs, and larger weights keep six blocks in flight per SM.
+// Piece i of thread t: box i & 1, row (t >> 3) + 32 (i >> 1), 16-byte chunk t & 7, so the eight
+// threads of each quarter-warp read eight different chunks of one 128-byte row (no bank
+// conflicts).  The copy wait is bounded; on a timeout the CTA records it and leaves.
 template <bool POW2>
-__global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                                  int64_t cols, uint8_t* __restrict__ q,
-                                                                  float* __restrict__ s) {
+__global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                  int64_t rows, int64_t cols,
+                                                                  uint8_t* __restrict__ q, float* __restrict__ s) {
+  __shared__ __align__(128) uint8_t tile[2 * 128 * 128];
+  __shared__ uint64_t full;
   __shared__ uint32_t wmax[8];
+  __shared__ int abort_flag;
   const int64_t nbc = cols >> 7;
   const int64_t br = blockIdx.x, bc = blockIdx.y;  // grid: x = block row, y = block column
   const int t = threadIdx.x;
-  const int lc = t & 15, r0 = t >> 4;
-  const uint16_t* xb = x + (br * 128) * cols + bc * 128;
-  uint4 v[8];
+  if (t == 0) {
+    abort_flag = 0;
+    mbar_init(&full, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&full, 2 * 128 * 128);
+    tma_load_2d(tile, &tmx, &full, static_cast<int32_t>(bc * 256), static_cast<int32_t>(br * 128));
+    tma_load_2d(tile + 128 * 128, &tmx, &full, static_cast<int32_t>(bc * 256 + 128), static_cast<int32_t>(br * 128));
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&full, 0, &abort_flag, kSiteQuantLoad);
+  if (__syncthreads_or(!ok)) {
+    if (t == 0) mbar_drain(&full, 0, 100000000ull);
+    return;
+  }
+  const int ch = t & 7, r0 = t >> 3;
   uint32_t m = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = ld_stream_v4(xb + static_cast<int64_t>(r0 + 16 * i) * cols + lc * 8);
-    m = max(m, absmax_bits8(v[i]));
-  }
+  for (int i = 0; i < 8; ++i)
+    m = max(m, absmax_bits8(*reinterpret_cast<const uint4*>(tile + (i & 1) * 16384 + (r0 + 32 * (i >> 1)) * 128 + ch * 16)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if ((t & 31) == 0) wmax[t >> 5] = m;
@@ -528,9 +547,11 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
   }
   const bool fast = QuotientBracket::usable(sc);
   const QuotientBracket qb(fast ? sc : 1.0f);
-#pragma unroll
+#pragma unroll 2
   for (int i = 0; i < 8; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    const int row = r0 + 32 * (i >> 1);
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + (i & 1) * 16384 + row * 128 + ch * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t p[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -538,7 +559,7 @@ __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const uint16_t
       if (POW2) p[j] = cvt_e4m3x2(__fmul_rn(a, inv), __fmul_rn(b, inv));
       else p[j] = fast ? e4m3x2_quotient(a, b, qb) : cvt_e4m3x2(__fdiv_rn(a, sc), __fdiv_rn(b, sc));
     }
-    *reinterpret_cast<uint2*>(q + (br * 128 + r0 + 16 * i) * cols + bc * 128 + lc * 8) =
+    *reinterpret_cast<uint2*>(q + (br * 128 + row) * cols + bc * 128 + (i & 1) * 64 + ch * 8) =
         make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
   }
   if (t == 0) s[br * nbc + bc] = sc;
