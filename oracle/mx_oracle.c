@@ -24,7 +24,7 @@
  *         sec 5.5 (MXFP4: E2M1 elements, 32-element blocks, one E8M0 scale),
  *         sec 5.6 (worked example), sec 7.1-7.4 (scale outside the sum, W4A4).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - E4M3 bias 7 / E5M2 bias 15 / E2M1 bias 1: the biases reproduce the
  *    printed max and min-subnormal values exactly.
  *  - Rounding is round-to-nearest, ties to the even code; results above the
