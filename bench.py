@@ -16,7 +16,8 @@ An extra group, not part of the default step, is measured with --only mx4:
        (row-wise, then row- and column-wise), against the unfused pair (bf16 fprop, then
        row-wise MX quantize of Y)
   moe  grouped GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
-       in multiples of 128, one launch (bf16 out), MXFP8 and NVFP4 (one global scale per expert)
+       in multiples of 128, one launch (bf16 out), MXFP8 and NVFP4 (one global scale per expert);
+       and the grouped NVFP4 quantization of the 8 experts' weights (one global scale each)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
        stochastic rounding (random bytes read from HBM), both, and 16x16 2-D blocks written in
        both orientations
@@ -85,6 +86,7 @@ W2DQ_BYTES = mx_q_bytes(14336, 4096)
 NVT_RHT_BYTES = nv_q_bytes(8192, 8192)
 NVT_SR_BYTES = nv_q_bytes(8192, 8192) + 8192 * 8192          # + one random byte per element
 NVT_2D_BYTES = 8192 * 8192 * (2 + 2 + 2 * (0.5 + 1 / 16))       # both orientations
+MOE4Q_BYTES = nv_q_bytes(len(MOE_SIZES) * 14336, 4096)           # every expert's weights, by groups
 
 
 def load_peaks():
@@ -246,7 +248,8 @@ class Workload:
             self.A9n = (u8(m9, 2048), u8(sb(m9, 4096, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
             self.B9n = (u8(n9, 2048), u8(sb(n9, 4096, 16, 1, mx.SCALE_UE4M3)), f32(len(MOE_SIZES)),
                         u8(16 * len(MOE_SIZES)))
-            self.launches_per_step += 2
+            self.woff9 = torch.arange(0, n9 + 1, 14336, dtype=torch.int64, device=dev)
+            self.launches_per_step += 4
             self._outs += [self.Y9]
         if "nvt" in groups:
             g8 = torch.Generator(device="cpu").manual_seed(8100)
@@ -331,13 +334,11 @@ class Workload:
                 mx.mx_quantize(d["A9"], layout=mx.ROWWISE, q_row=self.A9q[0], s_row=self.A9q[1])
                 mx.mx_quantize(d["B9"], layout=mx.ROWWISE, q_row=self.B9q[0], s_row=self.B9q[1])
                 self._moe_quantized = True
-                a, b = self.A9n, self.B9n
+                a = self.A9n
                 mx.nvfp4_quantize(d["A9"], q_packed=a[0], s_ue4m3=a[1], gscale=a[2], workspace=a[3])
-                per_expert = b[1].numel() // len(MOE_SIZES)        # scale bytes of 14336 rows
-                for e in range(len(MOE_SIZES)):
-                    mx.nvfp4_quantize(d["B9"][e * 14336:(e + 1) * 14336], q_packed=b[0][e * 14336:(e + 1) * 14336],
-                                      s_ue4m3=b[1][e * per_expert:(e + 1) * per_expert], gscale=b[2][e:e + 1],
-                                      workspace=b[3][16 * e:16 * (e + 1)])
+            mark("moe4q")
+            b = self.B9n                                          # each expert's weights: own global scale
+            mx.nvfp4_quantize_grouped(d["B9"], self.woff9, q_packed=b[0], s_ue4m3=b[1], gscale=b[2], workspace=b[3])
             mark("moegemm")
             mx.mx_gemm_grouped(self.A9q[0], self.A9q[1], mx.E4M3, self.B9q[0], self.B9q[1], mx.E4M3, self.off9,
                                sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
@@ -382,7 +383,8 @@ class Workload:
 
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
-             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moegemm", "moe4gemm", "fusedgemm", "fusedboth", "unfused"]
+             "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moe4q", "moegemm", "moe4gemm",
+             "fusedgemm", "fusedboth", "unfused"]
 
 
 def row_report(name, ms, peaks):
@@ -392,7 +394,7 @@ def row_report(name, ms, peaks):
     fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
     hbm_rows = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES,
                 "blkq": DSQ_BYTES, "blkconv": BLKCONV_BYTES, "w2dq": W2DQ_BYTES, "nvq_rht": NVT_RHT_BYTES,
-                "nvq_sr": NVT_SR_BYTES, "nvq_rht_sr": NVT_SR_BYTES, "nvq_2d": NVT_2D_BYTES}
+                "nvq_sr": NVT_SR_BYTES, "nvq_rht_sr": NVT_SR_BYTES, "nvq_2d": NVT_2D_BYTES, "moe4q": MOE4Q_BYTES}
     if name in hbm_rows:
         b = hbm_rows[name]
         gbs = b / s / 1e9
@@ -668,7 +670,8 @@ def main():
                "mxfp4_gemm": ["mx4gemm"], "mxfp4_quantize": ["mx4q"], "mx_gemm_blocks": ["blkgemm"],
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
-               "nvfp4_quantize_2d": ["nvq_2d"], "mx_gemm_grouped": ["moegemm"], "nvfp4_gemm_grouped": ["moe4gemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
+               "nvfp4_quantize_2d": ["nvq_2d"], "nvfp4_quantize_grouped": ["moe4q"], "mx_gemm_grouped": ["moegemm"],
+               "nvfp4_gemm_grouped": ["moe4gemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
                "mx_gemm_then_quantize": ["unfused"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
@@ -676,7 +679,8 @@ def main():
                 "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "mx_gemm_grouped": 1, "nvfp4_gemm_grouped": 1, "mx_gemm_mxout": 2,
+                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "nvfp4_quantize_grouped": 2, "mx_gemm_grouped": 1,
+                "nvfp4_gemm_grouped": 1, "mx_gemm_mxout": 2,
                 "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])

@@ -8,8 +8,8 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
-  mx_gemm_grouped, mx_gemm_mxout, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d, mx_scale_bytes,
-  nvfp4_workspace_bytes, mx_check.
+  mx_gemm_grouped, mx_gemm_mxout, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d,
+  nvfp4_quantize_grouped, nvfp4_gemm_grouped, mx_scale_bytes, nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
 
@@ -33,7 +33,7 @@ EXPORTS = (
     "nvfp4_quantize", "nvfp4_gemm", "fp8_blockwise_gemm", "mx_scale_bytes", "mx_check", "mx_num_sms",
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
     "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
-    "mx_selftest_wait_timeout", "mx_gemm_mxout_ex", "nvfp4_gemm_grouped",
+    "mx_selftest_wait_timeout", "mx_gemm_mxout_ex", "nvfp4_gemm_grouped", "nvfp4_quantize_grouped",
 )
 
 
@@ -85,6 +85,7 @@ def load():
             "mx_swizzle_scales": (i32, [vp, i64, i64, vp, vp]),
             "mx_selftest_wait_timeout": (i32, [i64, vp]),
             "nvfp4_gemm_grouped": (i32, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
+            "nvfp4_quantize_grouped": (i32, [vp, i64, i64, vp, i64, vp, vp, vp, vp, vp]),
             "mx_gemm_mxout_ex": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, vp, vp, i64, vp, vp, i64,
                                        vp]),
         }
@@ -258,6 +259,32 @@ def nvfp4_quantize(x: torch.Tensor, q_packed=None, s_ue4m3=None, gscale=None, wo
     st = load().nvfp4_quantize(_ptr(x), rows, cols, _ptr(q_packed), _ptr(s_ue4m3), _ptr(gscale),
                                _ptr(workspace), _stream(stream))
     _check(st, "nvfp4_quantize")
+    return q_packed, s_ue4m3, gscale
+
+
+def nvfp4_quantize_grouped(x: torch.Tensor, group_offsets: torch.Tensor, q_packed=None, s_ue4m3=None, gscale=None,
+                           workspace=None, stream=None):
+    """NVFP4 quantization of row groups of bf16 x[rows][cols], each group with its own global scale
+    (include/mx.h, nvfp4_quantize_grouped).  group_offsets: int64 CUDA tensor [G + 1].  Returns
+    (q_packed [rows][cols/2] u8, s_ue4m3 flat u8 in the NVFP4 GEMM layout, gscale float[G])."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bf16 tensor")
+    if group_offsets.dtype != torch.int64:
+        raise ValueError("group_offsets must be int64")
+    rows, cols = x.shape
+    dev = x.device
+    groups = group_offsets.numel() - 1
+    if q_packed is None:
+        q_packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+    if s_ue4m3 is None:
+        s_ue4m3 = _u8(mx_scale_bytes(rows, cols, 16, 1, SCALE_UE4M3), dev)
+    if gscale is None:
+        gscale = torch.empty(max(groups, 1), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _u8(max(16, (4 * groups + 15) // 16 * 16), dev)
+    st = load().nvfp4_quantize_grouped(_ptr(x), rows, cols, _ptr(group_offsets), groups, _ptr(q_packed),
+                                       _ptr(s_ue4m3), _ptr(gscale), _ptr(workspace), _stream(stream))
+    _check(st, "nvfp4_quantize_grouped")
     return q_packed, s_ue4m3, gscale
 
 

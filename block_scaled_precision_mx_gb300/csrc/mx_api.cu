@@ -644,6 +644,30 @@ mx_status nvfp4_quantize_ex(const void* x, int64_t rows, int64_t cols, int use_r
   return launch_status();
 }
 
+mx_status nvfp4_quantize_grouped(const void* x, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                                 int64_t groups, void* q_packed, void* s_ue4m3, float* gscale, void* workspace,
+                                 void* stream) {
+  if (!nvfp4_args_ok(x, rows, cols, 64, q_packed, s_ue4m3, gscale, workspace)) return MX_ERR_INVALID_ARG;
+  if (!group_offsets || !aligned(group_offsets, 8) || groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  auto* amax = static_cast<unsigned int*>(workspace);
+  const auto* xb = static_cast<const uint16_t*>(x);
+  const int g = static_cast<int>(groups);
+  if (cudaMemsetAsync(amax, 0, sizeof(unsigned int) * static_cast<size_t>(g), st) != cudaSuccess) return MX_ERR_CUDA;
+  const int sms = device_sms();
+  if (sms <= 0) return MX_ERR_CUDA;
+  int64_t grid1 = rows / 16;
+  if (grid1 > 8ll * sms) grid1 = 8ll * sms;
+  nvfp4_amax_grouped_kernel<<<static_cast<unsigned>(grid1), 256, 0, st>>>(xb, rows, cols, group_offsets, g, amax);
+  if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
+  dim3 grid;
+  if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
+  nvfp4_quantize_kernel<false, false, true><<<grid, 256, 0, st>>>(
+      xb, rows, cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3), gscale, amax, 0u, nullptr,
+      group_offsets, g);
+  return launch_status();
+}
+
 mx_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t cols, void* q_row, void* s_row, void* q_col,
                             void* s_col, float* gscale, void* workspace, void* stream) {
   if (!nvfp4_args_ok(x, rows, cols, 128, q_row, s_row, gscale, workspace)) return MX_ERR_INVALID_ARG;

@@ -671,26 +671,83 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
+// Grouped NVFP4 (row groups of one matrix quantized as tensors of their own, e.g. the weights of
+// MoE experts; "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 5.4 applied per group).
+// The group of row r: the last g < G with off[g] <= r.  Always in [0, G), whatever off holds, so
+// offsets that break their contract cannot send an access out of bounds.
+__device__ __forceinline__ int nv_group_of(const int64_t* __restrict__ off, int groups, int64_t r) {
+  int lo = 0, hi = groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Grouped pass 1: the maximum of each group (FP32 bits in amax[g], cleared by the host).  Work
+// unit = 16 rows (inside one group: offsets are multiples of 128); grid-stride over units.  CTA 0
+// also checks the offsets' contract (0 = off[0] <= ... <= off[G] = rows, multiples of 128) and
+// reports a broken one through the error word.
+__global__ void __launch_bounds__(256) nvfp4_amax_grouped_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                 int64_t cols, const int64_t* __restrict__ off,
+                                                                 int groups, unsigned int* __restrict__ amax) {
+  __shared__ uint32_t wmax[8];
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    bool good = __ldg(off) == 0 && __ldg(off + groups) == rows;
+    for (int g = 0; g < groups; ++g) {
+      const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
+      good = good && b >= a && (b & 127) == 0;
+    }
+    if (!good) atomicOr(&g_mx_error_word, kSiteBadGroups);
+  }
+  const int64_t units = rows >> 4;
+  const int64_t nvec = 2 * cols;  // 16 rows x cols / 8 vectors of 8
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const uint16_t* xu = x + u * 16 * cols;
+    uint32_t m = 0;
+    for (int64_t i = threadIdx.x; i < nvec; i += 256) m = max(m, absmax_bits8(ld_stream_v4(xu + i * 8)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 1; i < 8; ++i) m = max(m, wmax[i]);
+      atomicMax(amax + nv_group_of(off, groups, u * 16), m << 16);
+    }
+    __syncthreads();
+  }
+}
+
 // NVFP4 pass 2.  CTA = 32 rows x 128 columns; thread = one 16-element block.  RHT: the block is
 // transformed first (same signs as pass 1); SR: element codes by stochastic rounding of the IEEE
 // quotient with one random byte per element from rbits[rows][cols].
-template <bool RHT = false, bool SR = false>
+// GROUPED: amax_bits[G] and gscale[G] per row group (off[G + 1]); a CTA's 32 rows lie in one group.
+template <bool RHT = false, bool SR = false, bool GROUPED = false>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                              int64_t cols, uint8_t* __restrict__ qp,
                                                              uint8_t* __restrict__ sf, float* __restrict__ gscale,
                                                              const unsigned int* __restrict__ amax_bits,
-                                                             uint32_t signs = 0, const uint8_t* __restrict__ rbits = nullptr) {
+                                                             uint32_t signs = 0, const uint8_t* __restrict__ rbits = nullptr,
+                                                             const int64_t* __restrict__ off = nullptr, int groups = 1) {
   // grid: x = 32-row tile, y = 128-column tile; the last column tile may be half full
   // (cols % 128 == 64)
   __shared__ float s_glob[2];  // s_g and rcp(s_g), computed once per CTA
   const int64_t tr = blockIdx.x, tc = blockIdx.y;
   const int t = threadIdx.x;
   if (t == 0) {
-    const float amax = __uint_as_float(*amax_bits);
+    const int grp = GROUPED ? nv_group_of(off, groups, tr * 32) : 0;
+    const float amax = __uint_as_float(amax_bits[grp]);
     const float g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
     s_glob[0] = g;
     s_glob[1] = rcp_approx(g);
-    if (tr == 0 && tc == 0) *gscale = g;
+    if (!GROUPED && tr == 0 && tc == 0) *gscale = g;
+  }
+  if (GROUPED && tr == 0 && tc == 0) {  // every group's scale, empty groups included
+    for (int k = t; k < groups; k += 256) {
+      const float a = __uint_as_float(amax_bits[k]);
+      gscale[k] = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+    }
   }
   __syncthreads();
   const float sg = s_glob[0], rsg = s_glob[1];

@@ -298,6 +298,23 @@ mx_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols,
                          void* workspace, void* stream);
 
 /*
+ * nvfp4_quantize_grouped -- NVFP4 quantization of G row groups of one bf16 matrix, each group a
+ * tensor of its own (the weights or tokens of MoE experts; [NV] sec 5.4 applied per group): group
+ * g, rows off[g] <= r < off[g+1], gets its own amax and global scale gscale[g].  The results equal
+ * G calls of nvfp4_quantize on the groups' row slices, bit for bit: q_packed and s_ue4m3 hold the
+ * codes and scale chunks of the whole [rows][cols] matrix in the NVFP4 GEMM layout, group g's in
+ * its own rows (the layout nvfp4_gemm_grouped reads for B, whose gb is this gscale).
+ * group_offsets: device int64[G + 1], 0 = off[0] <= off[1] <= ... <= off[G] = rows, all multiples
+ * of 128; an empty group gets gscale 1.0.  Offsets that break this contract make the next
+ * mx_check() report MX_ERR_INVALID_ARG; the outputs are then unspecified, but no access leaves
+ * the caller's buffers.  gscale: device float[G]; workspace: 4 * G bytes (at least 16), 16-byte
+ * aligned, cleared by the call on `stream`.  1 <= G <= 1024, rows % 128 == 0, cols % 64 == 0.
+ */
+mx_status nvfp4_quantize_grouped(const void* x, int64_t rows, int64_t cols, const int64_t* group_offsets,
+                                 int64_t groups, void* q_packed, void* s_ue4m3, float* gscale, void* workspace,
+                                 void* stream);
+
+/*
  * nvfp4_gemm -- NVFP4 block-scaled GEMM.  [NV] sec 7.3-7.4:
  *   C[m][n] = gA * gB * sum_b sA[m][b] sB[n][b] sum_{i<16} qA qB, FP32 accumulate; the two
  *   global scales (device floats written by nvfp4_quantize) are applied in the epilogue.

@@ -169,6 +169,17 @@ def test_fused_output_ex_rejects_bad_arguments(lib):
     assert f(*b3, mx.BOTH, *ok_row, *ok_col, None) == mx.MX_ERR_UNSUPPORTED
 
 
+def test_nvfp4_quantize_grouped_rejects_bad_arguments(lib):
+    f = lib.nvfp4_quantize_grouped
+    ok = [FAKE, 256, 128, FAKE, 2, FAKE, FAKE, FAKE, FAKE, None]
+    for i, v, why in ((3, None, "no offsets"), (4, 0, "no groups"), (4, 1025, "too many groups"),
+                      (3, FAKE + 4, "offsets not 8-byte aligned"), (1, 192, "rows % 128"), (2, 96, "cols % 64"),
+                      (0, None, "no input"), (7, None, "no global scales"), (8, None, "no workspace"),
+                      (8, FAKE + 8, "workspace alignment")):
+        bad = list(ok); bad[i] = v
+        assert f(*bad) == mx.MX_ERR_INVALID_ARG, why
+
+
 def test_nvfp4_grouped_rejects_bad_arguments(lib):
     f = lib.nvfp4_gemm_grouped
     ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_F32, 256, None]

@@ -3,7 +3,10 @@ on SM120: software support" (xuesongtap.github.io), sec 1.2) against the CPU ora
 group: rows off[g] .. off[g+1] of A times the g-th [N][K] block of B, within |y - y_ref| <=
 1e-5 * sum_k |a_k b_k| (+ one bf16 ulp for bf16 output).  Covers groups whose rows end in half
 a 256-row tile, empty groups, one group equal to the plain GEMM, and offsets that break the
-contract (no work, MX_ERR_INVALID_ARG from mx_check).
+contract (no work, MX_ERR_INVALID_ARG from mx_check).  Also the NVFP4 experts: grouped NVFP4
+quantization (each row group a tensor of its own: codes, scales and global scale bit-identical to
+the oracle's quantization of that group's rows, "NVFP4: high accuracy with 4 bits"
+(theluyuan.com), sec 5.4), and the grouped NVFP4 product with per-expert global scales.
 """
 import numpy as np
 import pytest
@@ -160,3 +163,84 @@ def test_grouped_nvfp4_single_group_equals_plain_gemm():
     y2 = mx.nvfp4_gemm_grouped(*args, dev(np.array([0, M], np.int64)), M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
     assert torch.equal(y1, y2)
+
+
+# ------------------------------------------------------------------ grouped NVFP4 quantization
+from block_scaled_precision_mx_gb300 import synthetic  # noqa: E402
+
+
+def nv_grouped_input(sizes, cols, seed):
+    """bf16 rows of each group drawn at their own magnitude (and with sparse outliers), so every
+    group has its own amax and global scale."""
+    parts = [synthetic.with_sparse_outliers(n, cols, seed + g) * (4.0 ** (g % 5 - 2)) for g, n in enumerate(sizes) if n]
+    return torch.cat(parts).to(torch.bfloat16)
+
+
+def check_nv_grouped(x, sizes):
+    """Quantize x by groups on the GPU and compare every group with the oracle's quantization of
+    that group's rows as a tensor of its own (codes, scales, global scale bit for bit)."""
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    rows, cols = x.shape
+    q, s, g = mx.nvfp4_quantize_grouped(x.cuda(), dev(off))
+    assert mx.mx_check() == mx.MX_OK
+    qn, gn = q.cpu().numpy(), g.cpu().numpy()
+    sn = chunked_to_plain(s.cpu().numpy(), rows, cols // 16)
+    for k in range(len(sizes)):
+        lo, hi = int(off[k]), int(off[k + 1])
+        if hi == lo:
+            assert gn[k] == np.float32(1.0), f"empty group {k}: global scale {gn[k]}"
+            continue
+        oq, osc, og = orc.nv_quantize(x[lo:hi])
+        assert np.array_equal(qn[lo:hi], oq), f"group {k}: codes"
+        assert np.array_equal(sn[lo:hi], osc), f"group {k}: scales"
+        assert gn[k].view(np.uint32) == np.float32(og).view(np.uint32), f"group {k}: global scale"
+    return q, s, g, off
+
+
+def test_nvfp4_quantize_grouped_per_group_scales():
+    # uneven groups, an empty one, and a half-filled last 128-column tile (cols % 128 == 64)
+    check_nv_grouped(nv_grouped_input([384, 0, 128, 640], 320, 9100), [384, 0, 128, 640])
+
+
+def test_nvfp4_quantize_grouped_single_group():
+    check_nv_grouped(nv_grouped_input([512], 256, 9200), [512])
+
+
+def test_nvfp4_quantize_grouped_moe_weights_full_size():
+    # the MoE weights of the grouped-GEMM workload: 8 experts of 14336 x 4096, one global scale each
+    sizes = [14336] * 8
+    x = torch.cat([synthetic.normal(14336, 4096, 0.02 * (1 + e), 9300 + e) for e in range(8)])
+    check_nv_grouped(x, sizes)
+
+
+def test_nvfp4_quantize_grouped_feeds_grouped_gemm():
+    # experts' weights quantized by groups, tokens as one tensor, then the grouped product
+    sizes, N, K = [256, 128, 0, 384], 256, 512
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    a = synthetic.with_sparse_outliers(M, K, 9400)
+    w = nv_grouped_input([N] * G, K, 9500)
+    qa, sa, ga = mx.nvfp4_quantize(a.cuda())
+    qb, sb, gb, _ = check_nv_grouped(w, [N] * G)
+    y = mx.nvfp4_gemm_grouped(qa, sa, ga, qb, sb, gb, dev(off), M, N, K, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    oqa, osa, oga = orc.nv_quantize(a)
+    yn = y.cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        oqb, osb, ogb = orc.nv_quantize(w[g * N:(g + 1) * N])
+        ref, ab = orc.nv_gemm(oqa[lo:hi], osa[lo:hi], oga, oqb, osb, ogb)
+        assert_close(yn[lo:hi], ref, ab, bf16=False, what=f"expert {g}")
+
+
+@pytest.mark.parametrize("off", [[0, 100, 256], [0, 128], [0, 256, 128, 256]])
+def test_nvfp4_quantize_grouped_rejects_broken_offsets_on_the_device(off):
+    x = synthetic.normal(256, 128, 1.0, 9600).cuda()
+    offsets = dev(np.array(off, np.int64))
+    mx.nvfp4_quantize_grouped(x, offsets)
+    assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
+    # the context stays usable: a valid call right after is exact
+    check_nv_grouped(synthetic.normal(256, 128, 1.0, 9601), [128, 128])
