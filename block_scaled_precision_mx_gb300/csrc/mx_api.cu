@@ -493,7 +493,15 @@ mx_status mx_gemm_grouped(const void* qa, const void* sa, mx_elem ea, const void
 mx_status nvfp4_gemm_grouped(const void* qa, const void* sa, const float* ga, const void* qb, const void* sb,
                              const float* gb, const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N,
                              int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  return nvfp4_gemm_grouped_ex(qa, sa, ga, 0, qb, sb, gb, group_offsets, groups, M, N, K, out, out_dtype, ldc, stream);
+}
+
+mx_status nvfp4_gemm_grouped_ex(const void* qa, const void* sa, const float* ga, int ga_per_group, const void* qb,
+                                const void* sb, const float* gb, const int64_t* group_offsets, int64_t groups,
+                                int64_t M, int64_t N, int64_t K, void* out, mx_out out_dtype, int64_t ldc,
+                                void* stream) {
   if (!qa || !sa || !ga || !qb || !sb || !gb || !out || !group_offsets) return MX_ERR_INVALID_ARG;
+  if (ga_per_group != 0 && ga_per_group != 1) return MX_ERR_INVALID_ARG;
   if (groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
   if (!gemm_shape_ok(M, N, K, 256, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
   if (groups * N > (1ll << 30)) return MX_ERR_INVALID_ARG;
@@ -505,6 +513,7 @@ mx_status nvfp4_gemm_grouped(const void* qa, const void* sa, const float* ga, co
   a.sfb = static_cast<const uint8_t*>(sb);
   a.ga = ga;
   a.gb = gb;
+  a.ga_stride = ga_per_group;
   a.out = out;
   a.ldc = ldc;
   a.M = static_cast<int>(M);

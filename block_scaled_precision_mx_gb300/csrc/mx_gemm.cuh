@@ -92,6 +92,7 @@ struct GemmArgs {
   const float* dsb;  // DeepSeek: float[N/128][K/128]
   const float* ga;   // NVFP4 global scales
   const float* gb;
+  int ga_stride;     // grouped NVFP4: 0 = one global scale of A, 1 = one per group (ga[g])
   void* out;
   int64_t ldc;
   int M, N, K;  // K in elements (grouped: M = rows of all groups)

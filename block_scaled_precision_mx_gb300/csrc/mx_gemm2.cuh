@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
       int rows_valid, nb, grp;
       decode(tile, a_row0, b_row0, rows_valid, nb, grp);
       // grouped NVFP4: every expert's B carries its own global scale
-      if (KIND == kNvf4 && GROUPED) gscale = __fmul_rn(*args.ga, __ldg(args.gb + grp));
+      if (KIND == kNvf4 && GROUPED) gscale = __fmul_rn(__ldg(args.ga + grp * args.ga_stride), __ldg(args.gb + grp));
       const bool store = static_cast<int>(rank) * Cfg::ROWS < rows_valid;  // this CTA's rows exist
       bool ok = mbar_wait(tfull_bar, acc_it & 1, abort_flag, kSiteEpiTmemFull);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;

@@ -278,6 +278,18 @@ mx_status nvfp4_gemm_grouped(const void* qa, const void* sa, const float* ga, co
                              const float* gb, const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N,
                              int64_t K, void* out, mx_out out_dtype, int64_t ldc, void* stream);
 
+/*
+ * nvfp4_gemm_grouped_ex -- nvfp4_gemm_grouped with, when ga_per_group == 1, one global scale of A
+ * per group: ga is then a device float[G] and group g's results are scaled by ga[g] * gb[g] (the
+ * tokens routed to each expert quantized as a tensor of their own, e.g. by nvfp4_quantize_grouped
+ * with the same offsets).  ga_per_group == 0 is nvfp4_gemm_grouped; any other value returns
+ * MX_ERR_INVALID_ARG.
+ */
+mx_status nvfp4_gemm_grouped_ex(const void* qa, const void* sa, const float* ga, int ga_per_group, const void* qb,
+                                const void* sb, const float* gb, const int64_t* group_offsets, int64_t groups,
+                                int64_t M, int64_t N, int64_t K, void* out, mx_out out_dtype, int64_t ldc,
+                                void* stream);
+
 /* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
 

@@ -180,6 +180,15 @@ def test_nvfp4_quantize_grouped_rejects_bad_arguments(lib):
         assert f(*bad) == mx.MX_ERR_INVALID_ARG, why
 
 
+def test_nvfp4_grouped_ex_rejects_bad_arguments(lib):
+    f = lib.nvfp4_gemm_grouped_ex
+    ok = [FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_F32, 256, None]
+    for i, v, why in ((3, 2, "ga_per_group not 0 or 1"), (3, -1, "ga_per_group not 0 or 1"), (2, None, "no ga"),
+                      (8, 0, "no groups"), (7, FAKE + 4, "offsets alignment"), (11, 128, "K % 256")):
+        bad = list(ok); bad[i] = v
+        assert f(*bad) == mx.MX_ERR_INVALID_ARG, why
+
+
 def test_nvfp4_grouped_rejects_bad_arguments(lib):
     f = lib.nvfp4_gemm_grouped
     ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_F32, 256, None]

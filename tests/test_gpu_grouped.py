@@ -244,3 +244,27 @@ def test_nvfp4_quantize_grouped_rejects_broken_offsets_on_the_device(off):
     assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
     # the context stays usable: a valid call right after is exact
     check_nv_grouped(synthetic.normal(256, 128, 1.0, 9601), [128, 128])
+
+
+def test_nvfp4_grouped_gemm_per_expert_token_scales():
+    # the routed tokens quantized by expert (one global scale per expert's tokens) and the experts'
+    # weights by expert: group g's results scaled by ga[g] * gb[g]
+    sizes, N, K = [384, 0, 128, 256], 256, 512
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    a = nv_grouped_input(sizes, K, 9700)
+    w = nv_grouped_input([N] * G, K, 9800)
+    qa, sa, ga, _ = check_nv_grouped(a, sizes)
+    qb, sb, gb, _ = check_nv_grouped(w, [N] * G)
+    y = mx.nvfp4_gemm_grouped_ex(qa, sa, ga, True, qb, sb, gb, dev(off), M, N, K, out_dtype=mx.OUT_BF16)
+    assert mx.mx_check() == mx.MX_OK
+    yn = y.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        oqa, osa, oga = orc.nv_quantize(a[lo:hi])
+        oqb, osb, ogb = orc.nv_quantize(w[g * N:(g + 1) * N])
+        ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb)
+        assert_close(yn[lo:hi], ref, ab, bf16=True, what=f"expert {g}")
