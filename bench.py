@@ -17,7 +17,8 @@ An extra group, not part of the default step, is measured with --only mx4:
        row-wise MX quantize of Y)
   moe  grouped GEMM: 8 experts (K=4096 -> N=14336 each), 16384 routed rows split unevenly
        in multiples of 128, one launch (bf16 out), MXFP8 and NVFP4 (one global scale per expert);
-       and the grouped NVFP4 quantization of the 8 experts' weights (one global scale each)
+       and the grouped NVFP4 quantization of the 8 experts' weights (one global scale each); the
+       same experts as DeepSeek FP8 (1x128 token tiles, 128x128 weight blocks, promotion per 128)
   nvt  NVFP4 training options on one 8192x8192 tensor: the 16-point random Hadamard transform,
        stochastic rounding (random bytes read from HBM), both, and 16x16 2-D blocks written in
        both orientations
@@ -249,7 +250,10 @@ class Workload:
             self.B9n = (u8(n9, 2048), u8(sb(n9, 4096, 16, 1, mx.SCALE_UE4M3)), f32(len(MOE_SIZES)),
                         u8(16 * len(MOE_SIZES)))
             self.woff9 = torch.arange(0, n9 + 1, 14336, dtype=torch.int64, device=dev)
-            self.launches_per_step += 4
+            # DeepSeek FP8 experts: tokens in 1x128 tiles, the stacked weights in 128x128 blocks
+            self.A9d = (u8(m9, 4096), f32(4096 // 128, m9))
+            self.B9d = (u8(n9, 4096), f32(n9 // 128, 4096 // 128))
+            self.launches_per_step += 5
             self._outs += [self.Y9]
         if "nvt" in groups:
             g8 = torch.Generator(device="cpu").manual_seed(8100)
@@ -336,6 +340,10 @@ class Workload:
                 self._moe_quantized = True
                 a = self.A9n
                 mx.nvfp4_quantize(d["A9"], q_packed=a[0], s_ue4m3=a[1], gscale=a[2], workspace=a[3])
+                mx.mx_quantize(d["A9"], block=128, block_rows=1, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                               q_row=self.A9d[0], s_row=self.A9d[1])
+                mx.mx_quantize(d["B9"], block=128, block_rows=128, sfmt=mx.SCALE_FP32, layout=mx.ROWWISE,
+                               q_row=self.B9d[0], s_row=self.B9d[1])
             mark("moe4q")
             b = self.B9n                                          # each expert's weights: own global scale
             mx.nvfp4_quantize_grouped(d["B9"], self.woff9, q_packed=b[0], s_ue4m3=b[1], gscale=b[2], workspace=b[3])
@@ -345,6 +353,9 @@ class Workload:
             mark("moe4gemm")
             mx.nvfp4_gemm_grouped(self.A9n[0], self.A9n[1], self.A9n[2], self.B9n[0], self.B9n[1], self.B9n[2],
                                   self.off9, sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
+            mark("moedsgemm")
+            mx.fp8_blockwise_gemm_grouped(self.A9d[0], self.A9d[1], self.B9d[0], self.B9d[1], self.off9,
+                                          sum(MOE_SIZES), 14336, 4096, mx.OUT_BF16, out=self.Y9)
         if "nvt" in g:
             q = self.A8q
             mark("nvq_rht")
@@ -384,7 +395,7 @@ class Workload:
 
 ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "dsgemm", "blkq", "blkconv", "blkgemm",
              "w2dq", "mx4q", "mx4gemm", "nvq_rht", "nvq_sr", "nvq_rht_sr", "nvq_2d", "moe4q", "moegemm", "moe4gemm",
-             "fusedgemm", "fusedboth", "unfused"]
+             "moedsgemm", "fusedgemm", "fusedboth", "unfused"]
 
 
 def row_report(name, ms, peaks):
@@ -401,8 +412,8 @@ def row_report(name, ms, peaks):
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
     f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN,
-         "unfused": F_LIN}[name]
+         "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "moedsgemm": F_MOE, "fusedgemm": F_LIN,
+         "fusedboth": F_LIN, "unfused": F_LIN}[name]
     tf = f / s / 1e12
     peak = fp4_peak if name in ("nvgemm", "mx4gemm", "moe4gemm") else fp8_peak
     return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
@@ -661,7 +672,8 @@ def main():
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
     row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "fusedgemm": F_LIN, "fusedboth": F_LIN}
+                 "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "moedsgemm": F_MOE, "fusedgemm": F_LIN,
+                 "fusedboth": F_LIN}
     step_flops = sum(row_flops.get(n, 0) for n in present)
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
@@ -671,7 +683,8 @@ def main():
                "pow2_block_quantize": ["blkq"], "mx_scales_from_fp32_blocks": ["blkconv"],
                "mx_quantize_2d32": ["w2dq"], "nvfp4_quantize_ex": ["nvq_rht", "nvq_sr", "nvq_rht_sr"],
                "nvfp4_quantize_2d": ["nvq_2d"], "nvfp4_quantize_grouped": ["moe4q"], "mx_gemm_grouped": ["moegemm"],
-               "nvfp4_gemm_grouped": ["moe4gemm"], "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
+               "nvfp4_gemm_grouped": ["moe4gemm"], "fp8_blockwise_gemm_grouped": ["moedsgemm"],
+               "mx_gemm_mxout": ["fusedgemm", "fusedboth"],
                "mx_gemm_then_quantize": ["unfused"]}
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
@@ -680,7 +693,7 @@ def main():
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
                 "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "nvfp4_quantize_grouped": 2, "mx_gemm_grouped": 1,
-                "nvfp4_gemm_grouped": 1, "mx_gemm_mxout": 2,
+                "nvfp4_gemm_grouped": 1, "fp8_blockwise_gemm_grouped": 1, "mx_gemm_mxout": 2,
                 "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
     dom_ms = sum(rows_ms[r] for r in kernels[dom])
@@ -690,12 +703,13 @@ def main():
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
-    if dom in ("mx_gemm", "nvfp4_gemm", "fp8_blockwise_gemm", "mxfp4_gemm", "mx_gemm_blocks", "mx_gemm_grouped",
-               "mx_gemm_mxout", "mx_gemm_then_quantize"):
-        flops = {"mx_gemm": len(kernels[dom]) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
-                 "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE, "mx_gemm_mxout": F_LIN,
-                 "mx_gemm_then_quantize": F_LIN}[dom]
-        fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm")
+    gemm_flops = {"mx_gemm": len(kernels.get("mx_gemm", [])) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
+                  "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE, "nvfp4_gemm_grouped": F_MOE,
+                  "fp8_blockwise_gemm_grouped": F_MOE, "mx_gemm_mxout": len(kernels.get("mx_gemm_mxout", [])) * F_LIN,
+                  "mx_gemm_then_quantize": F_LIN}
+    if dom in gemm_flops:
+        flops = gemm_flops[dom]
+        fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm", "nvfp4_gemm_grouped")
         peak = 3 * fp8_peak if fp4 else fp8_peak
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),

@@ -9,8 +9,8 @@ is no CPU fallback: if the library cannot be loaded, every call raises.
 Entry points (same names as the C ABI):
   mx_quantize, mx_quantize_dual, mx_gemm, nvfp4_quantize, nvfp4_gemm, fp8_blockwise_gemm,
   mx_gemm_grouped, mx_gemm_mxout, mx_scales_from_fp32_blocks, nvfp4_quantize_ex, nvfp4_quantize_2d,
-  nvfp4_quantize_grouped, nvfp4_gemm_grouped, nvfp4_gemm_grouped_ex, mx_scale_bytes, nvfp4_workspace_bytes,
-  mx_check.
+  nvfp4_quantize_grouped, nvfp4_gemm_grouped, nvfp4_gemm_grouped_ex, fp8_blockwise_gemm_grouped, mx_scale_bytes,
+  nvfp4_workspace_bytes, mx_check.
 """
 from __future__ import annotations
 
@@ -35,7 +35,7 @@ EXPORTS = (
     "nvfp4_quantize_noalloc", "mx_quantize_dual", "mx_scales_from_fp32_blocks", "nvfp4_quantize_ex",
     "nvfp4_quantize_2d", "mx_gemm_grouped", "mx_gemm_mxout", "mx_unswizzle_scales", "mx_swizzle_scales",
     "mx_selftest_wait_timeout", "mx_gemm_mxout_ex", "nvfp4_gemm_grouped", "nvfp4_quantize_grouped",
-    "nvfp4_gemm_grouped_ex",
+    "nvfp4_gemm_grouped_ex", "fp8_blockwise_gemm_grouped",
 )
 
 
@@ -89,6 +89,7 @@ def load():
             "nvfp4_gemm_grouped": (i32, [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
             "nvfp4_quantize_grouped": (i32, [vp, i64, i64, vp, i64, vp, vp, vp, vp, vp]),
             "nvfp4_gemm_grouped_ex": (i32, [vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
+            "fp8_blockwise_gemm_grouped": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, i32, i64, vp]),
             "mx_gemm_mxout_ex": (i32, [vp, vp, i32, vp, vp, i32, i64, i64, i64, i32, i32, vp, vp, i64, vp, vp, i64,
                                        vp]),
         }
@@ -438,6 +439,20 @@ def nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=OUT_F32, out=None, str
     st = load().nvfp4_gemm(_ptr(qa), _ptr(sa), _ptr(ga), _ptr(qb), _ptr(sb), _ptr(gb), M, N, K, out.data_ptr(),
                            out_dtype, ldc, _stream(stream))
     _check(st, "nvfp4_gemm")
+    return out
+
+
+def fp8_blockwise_gemm_grouped(qa, sa, qb, sb, group_offsets, M, N, K, out_dtype=OUT_BF16, out=None, stream=None):
+    """DeepSeek FP8 grouped GEMM (include/mx.h, fp8_blockwise_gemm_grouped): rows off[g] .. off[g+1] of
+    A times the g-th [N][K] block of B, FP32 promotion every 128 of K.  sa float [K/128][M] (1x128
+    tiles), sb float [G*N/128][K/128] (128x128 blocks of the stacked weights)."""
+    if group_offsets.dtype != torch.int64:
+        raise ValueError("group_offsets must be int64")
+    out, ldc = _out(M, N, out_dtype, out, qa.device)
+    st = load().fp8_blockwise_gemm_grouped(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), _ptr(group_offsets),
+                                           group_offsets.numel() - 1, M, N, K, out.data_ptr(), out_dtype, ldc,
+                                           _stream(stream))
+    _check(st, "fp8_blockwise_gemm_grouped")
     return out
 
 

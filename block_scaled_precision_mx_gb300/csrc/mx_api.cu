@@ -181,17 +181,18 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
 }
 
 // DeepSeek CTA-pair kernel, 256 x 256 output tiles.
-template <bool OUT_BF16>
-mx_status launch_ds_gemm2(const void* qa, const void* qb, const GemmArgs& args, cudaStream_t st) {
-  using Cfg = Ds2Cfg<OUT_BF16>;
+template <bool OUT_BF16, bool GROUPED = false>
+mx_status launch_ds_gemm2(const void* qa, const void* qb, const GemmArgs& args, cudaStream_t st, int64_t b_rows = 0) {
+  using Cfg = Ds2Cfg<OUT_BF16, GROUPED>;
   static int max_clusters[64] = {};
   CUtensorMap ta, tb, tout;
   if (!make_tmap(&ta, qa, args.M, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
-  if (!make_tmap(&tb, qb, args.N, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
+  if (!make_tmap(&tb, qb, GROUPED ? b_rows : args.N, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_out_tmap(&tout, args.out, args.M, args.N, args.ldc, OUT_BF16)) return MX_ERR_CUDA;
-  const int tiles = (args.M / Cfg::BM) * (args.N / Cfg::BN);
-  return launch_pairs(ds_gemm2_kernel<OUT_BF16>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters, st, ta, tb,
-                      tout, args);
+  // grouped: the tile count is known on the device only; every co-resident cluster runs
+  const int tiles = GROUPED ? 0x7FFFFFFF : (args.M / Cfg::BM) * (args.N / Cfg::BN);
+  return launch_pairs(ds_gemm2_kernel<OUT_BF16, GROUPED>, Cfg::THREADS, Cfg::SMEM_BYTES, tiles, max_clusters, st,
+                      ta, tb, tout, args);
 }
 
 // MX quantize launch: nf = 1 (format f0) or 2 (E4M3 and E5M2 from one read).
@@ -747,6 +748,32 @@ mx_status fp8_blockwise_gemm(const void* qa, const float* sa, const void* qb, co
   a.idesc = make_idesc_f8f6f4(0u, 0u, 128, 128);
   if (out_dtype == MX_OUT_BF16) return launch_gemm<kDsF8, 128, true>(qa, qb, K, a, st);
   return launch_gemm<kDsF8, 128, false>(qa, qb, K, a, st);
+}
+
+mx_status fp8_blockwise_gemm_grouped(const void* qa, const float* sa, const void* qb, const float* sb,
+                                     const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N, int64_t K,
+                                     void* out, mx_out out_dtype, int64_t ldc, void* stream) {
+  if (!qa || !sa || !qb || !sb || !out || !group_offsets) return MX_ERR_INVALID_ARG;
+  if (groups < 1 || groups > kMaxGroups) return MX_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(M, N, K, 128, ldc, out_dtype) || N % 256) return MX_ERR_INVALID_ARG;
+  if (groups * N > (1ll << 30)) return MX_ERR_INVALID_ARG;
+  if (!aligned(qa, 16) || !aligned(qb, 16) || !aligned(sa, 4) || !aligned(sb, 4) || !aligned(out, 16) ||
+      !aligned(group_offsets, 8))
+    return MX_ERR_INVALID_ARG;
+  GemmArgs a{};
+  a.dsa = sa;
+  a.dsb = sb;
+  a.out = out;
+  a.ldc = ldc;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.group_off = group_offsets;
+  a.groups = static_cast<int>(groups);
+  a.idesc = make_idesc_f8f6f4(0u, 0u, 256, 256);
+  cudaStream_t st = as_stream(stream);
+  if (out_dtype == MX_OUT_BF16) return launch_ds_gemm2<true, true>(qa, qb, a, st, groups * N);
+  return launch_ds_gemm2<false, true>(qa, qb, a, st, groups * N);
 }
 
 mx_status mx_check(void* stream) {

@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
 // (Measured: 32-column pieces with registers moved from the control warps to the epilogue by
 // setmaxnreg ran 12% slower at 4096 x 2048 x 7168.)
 // ---------------------------------------------------------------------------------------------
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool GROUPED_ = false>
 struct Ds2Cfg {
   static constexpr int BM = 256;
   static constexpr int BN = 256;
@@ -543,7 +543,8 @@ struct Ds2Cfg {
   static constexpr int BAR_BYTES = 1024;
   static constexpr int CHUNK_BYTES = OUT_BF16 ? 2048 : 4096;
   static constexpr int STAGING = 8 * CHUNK_BYTES + 1024;
-  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING) / STAGE_BYTES;
+  static constexpr int STATIC_SMEM = GROUPED_ ? (kMaxGroups + 1) * 4 + 64 : 64;  // group table
+  static constexpr int STAGES_RAW = (kSmemLimit - 1024 - BAR_BYTES - STAGING - STATIC_SMEM) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING + BAR_BYTES;
   static constexpr int NUM_MMA = KBYTES / 32;
@@ -557,11 +558,15 @@ struct Ds2Cfg {
   static_assert(NBUF * BUF_COLS <= TMEM_COLS, "TMEM overflow");
 };
 
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
+// GROUPED: the DeepSeek expert products of a mixture-of-experts layer in one launch (as for the
+// block-scaled kernel: rows off[g] .. off[g+1] of A times the g-th [N][K] block of B, whose
+// 128x128 block scales are rows g N / 128 .. of sB; a CTA whose 128 rows lie past its group's
+// last row computes but stores nothing).
+template <bool OUT_BF16, bool GROUPED = false>
+__global__ void __launch_bounds__(Ds2Cfg<OUT_BF16, GROUPED>::THREADS, 1)
     ds_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
-  using Cfg = Ds2Cfg<OUT_BF16>;
+  using Cfg = Ds2Cfg<OUT_BF16, GROUPED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -584,8 +589,50 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
   const int nclusters = gridDim.x >> 1;
   const int num_mb = args.M / Cfg::BM;
   const int num_nb = args.N / Cfg::BN;
-  const int num_tiles = num_mb * num_nb;
   const int num_kt = args.K / 128;
+  __shared__ int grp_start[GROUPED ? kMaxGroups + 1 : 1];  // first tile of each group
+  if (GROUPED && threadIdx.x == 0) {
+    // offsets must start at 0, end at M, be multiples of 128 and never decrease; otherwise no
+    // tile runs and the error word reports it
+    const int64_t* off = args.group_off;
+    bool good = __ldg(off) == 0 && __ldg(off + args.groups) == args.M;
+    int t = 0;
+    for (int g = 0; g < args.groups; ++g) {
+      grp_start[g] = t;
+      const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
+      good = good && a >= 0 && b >= a && (a & 127) == 0 && (b & 127) == 0 && b <= args.M;
+      if (good) t += static_cast<int>((b - a + Cfg::BM - 1) / Cfg::BM) * num_nb;
+    }
+    if (!good) {
+      t = 0;
+      if (blockIdx.x == 0) atomicOr(&g_mx_error_word, kSiteBadGroups);
+    }
+    grp_start[args.groups] = t;
+  }
+  // tile -> first A row of the pair, first B row (of the stacked experts), rows of the group from
+  // a_row0 on, n-block
+  auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb) {
+    int mb;
+    if (GROUPED) {
+      int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (grp_start[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+      }
+      const int64_t off = __ldg(args.group_off + lo), rows_g = __ldg(args.group_off + lo + 1) - off;
+      tile_coords(tile - grp_start[lo], static_cast<int>((rows_g + Cfg::BM - 1) / Cfg::BM), num_nb, mb, nb);
+      a_row0 = off + static_cast<int64_t>(mb) * Cfg::BM;
+      b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * Cfg::BN;
+      const int64_t left = rows_g - static_cast<int64_t>(mb) * Cfg::BM;
+      rows_valid = left < Cfg::BM ? static_cast<int>(left) : Cfg::BM;
+    } else {
+      tile_coords(tile, num_mb, num_nb, mb, nb);
+      a_row0 = static_cast<int64_t>(mb) * Cfg::BM;
+      b_row0 = static_cast<int64_t>(nb) * Cfg::BN;
+      rows_valid = Cfg::BM;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -611,6 +658,7 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -619,10 +667,11 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
       long issued = 0;
       bool ok = true;
       for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-        int mb, nb;
-        tile_coords(tile, num_mb, num_nb, mb, nb);
-        const int a_row = mb * Cfg::BM + static_cast<int>(rank) * Cfg::ROWS;
-        const int b_row = nb * Cfg::BN + static_cast<int>(rank) * Cfg::ROWS;
+        int64_t a_row0, b_row0;
+        int rows_valid, nb;
+        decode(tile, a_row0, b_row0, rows_valid, nb);
+        const int a_row = static_cast<int>(a_row0) + static_cast<int>(rank) * Cfg::ROWS;
+        const int b_row = static_cast<int>(b_row0) + static_cast<int>(rank) * Cfg::ROWS;
         for (int kt = 0; kt < num_kt; ++kt) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag, kSiteProducerEmpty)) {
             ok = false;
@@ -699,11 +748,15 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
     uint32_t acc_it = 0;
     bool ok = true;
     for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
-      int mb, nb;
-      tile_coords(tile, num_mb, num_nb, mb, nb);
-      const int32_t row0 = mb * Cfg::BM + static_cast<int32_t>(rank) * Cfg::ROWS + q * 32;
-      const float* sa_row = args.dsa + row0 + lane;
-      const float* sb_blk = args.dsb + static_cast<int64_t>(2 * nb + half) * kbs;
+      int64_t a_row0, b_row0;
+      int rows_valid, nb;
+      decode(tile, a_row0, b_row0, rows_valid, nb);
+      const bool store = static_cast<int>(rank) * Cfg::ROWS < rows_valid;  // this CTA's rows exist
+      const int32_t row0 = static_cast<int32_t>(a_row0) + static_cast<int32_t>(rank) * Cfg::ROWS + q * 32;
+      // (rows past M, in a grouped tile's unused half, read row M - 1's scales: never stored)
+      const int64_t srow = row0 + lane < args.M ? row0 + lane : args.M - 1;
+      const float* sa_row = args.dsa + srow;
+      const float* sb_blk = args.dsb + (b_row0 / 128 + half) * kbs;
       float nsa = __ldg(sa_row), nsb = __ldg(sb_blk);
       uint64_t acc[64];  // this thread's 128 FP32 accumulators as pairs
 #pragma unroll
@@ -746,6 +799,7 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16>::THREADS, 1)
         ++acc_it;
       }
       if (!ok) break;
+      if (!store) continue;
       // the tile's 32 rows x 128 columns, as four 32 x 32 TMA stores through the staging buffer
 #pragma unroll
       for (int c = 0; c < 4; ++c) {

@@ -290,6 +290,20 @@ mx_status nvfp4_gemm_grouped_ex(const void* qa, const void* sa, const float* ga,
                                 int64_t M, int64_t N, int64_t K, void* out, mx_out out_dtype, int64_t ldc,
                                 void* stream);
 
+/*
+ * fp8_blockwise_gemm_grouped -- the DeepSeek FP8 expert GEMMs of a mixture-of-experts layer in one
+ * launch ([DS] sec 5, 6.3; group layout as mx_gemm_grouped): group g computes, for its rows
+ * off[g] <= m < off[g+1], C[m][n] = sum_kb sA[kb][m] sB[gN/128 + n/128][kb] P_kb[m][n], with P_kb
+ * the exact FP32 sum of qA qB over k-block kb (promotion every 128 of K, as fp8_blockwise_gemm).
+ * qa[M][K] E4M3 with sa float[K/128][M] (1x128 tiles); qb[G*N][K] E4M3, the experts' [N][K]
+ * weights stacked, with sb float[G*N/128][K/128] (their 128x128 blocks stacked the same way, as
+ * one mx_quantize(block=128, block_rows=128) of the stacked weights gives).  group_offsets as
+ * mx_gemm_grouped.  M % 128 == 0, N % 256 == 0, K % 128 == 0, 1 <= G <= 1024; out as for mx_gemm.
+ */
+mx_status fp8_blockwise_gemm_grouped(const void* qa, const float* sa, const void* qb, const float* sb,
+                                     const int64_t* group_offsets, int64_t groups, int64_t M, int64_t N, int64_t K,
+                                     void* out, mx_out out_dtype, int64_t ldc, void* stream);
+
 /* Bytes of caller-owned device workspace nvfp4_quantize needs (>= 16). */
 size_t nvfp4_workspace_bytes(int64_t rows, int64_t cols);
 

@@ -189,6 +189,16 @@ def test_nvfp4_grouped_ex_rejects_bad_arguments(lib):
         assert f(*bad) == mx.MX_ERR_INVALID_ARG, why
 
 
+def test_ds_grouped_rejects_bad_arguments(lib):
+    f = lib.fp8_blockwise_gemm_grouped
+    ok = [FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_BF16, 256, None]
+    for i, v, why in ((4, None, "no offsets"), (5, 0, "no groups"), (5, 1025, "too many groups"),
+                      (7, 128, "N % 256"), (8, 64, "K % 128"), (6, 192, "M % 128"), (4, FAKE + 4, "offsets alignment"),
+                      (1, FAKE + 2, "scale alignment"), (0, None, "no A")):
+        bad = list(ok); bad[i] = v
+        assert f(*bad) == mx.MX_ERR_INVALID_ARG, why
+
+
 def test_nvfp4_grouped_rejects_bad_arguments(lib):
     f = lib.nvfp4_gemm_grouped
     ok = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 256, 256, 256, FAKE, mx.OUT_F32, 256, None]

@@ -6,7 +6,9 @@ a 256-row tile, empty groups, one group equal to the plain GEMM, and offsets tha
 contract (no work, MX_ERR_INVALID_ARG from mx_check).  Also the NVFP4 experts: grouped NVFP4
 quantization (each row group a tensor of its own: codes, scales and global scale bit-identical to
 the oracle's quantization of that group's rows, "NVFP4: high accuracy with 4 bits"
-(theluyuan.com), sec 5.4), and the grouped NVFP4 product with per-expert global scales.
+(theluyuan.com), sec 5.4), and the grouped NVFP4 product with per-expert global scales; and the
+DeepSeek FP8 expert products with FP32 promotion per 128 of K ("Why FP8 training is stable"
+(magicnetworld.com), sec 6.3), each expert's 128x128 weight-block scales its own rows of sB.
 """
 import numpy as np
 import pytest
@@ -268,3 +270,61 @@ def test_nvfp4_grouped_gemm_per_expert_token_scales():
         oqb, osb, ogb = orc.nv_quantize(w[g * N:(g + 1) * N])
         ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb)
         assert_close(yn[lo:hi], ref, ab, bf16=True, what=f"expert {g}")
+
+
+# ------------------------------------------------------------------ grouped DeepSeek FP8
+def ds_grouped_operands(M, G, N, K, seed):
+    rng = np.random.default_rng(seed)
+    sign = lambda shape: rng.integers(0, 2, shape, dtype=np.uint8) << 7
+    qa = rng.integers(0, 0x7E, (M, K), dtype=np.uint8) | sign((M, K))
+    qb = rng.integers(0, 0x7E, (G * N, K), dtype=np.uint8) | sign((G * N, K))
+    sa = (rng.random((M, K // 128)) * 0.01 + 0.001).astype(np.float32)             # [M][K/128]
+    sb = (rng.random((G * N // 128, K // 128)) * 0.01 + 0.001).astype(np.float32)   # [G N/128][K/128]
+    return qa, sa, qb, sb
+
+
+def run_ds_grouped(sizes, N, K, out_dtype, seed, sample=None):
+    G = len(sizes)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    qa, sa, qb, sb = ds_grouped_operands(M, G, N, K, seed)
+    y = mx.fp8_blockwise_gemm_grouped(dev(qa), dev(sa.T), dev(qb), dev(sb), dev(off), M, N, K, out_dtype=out_dtype)
+    assert mx.mx_check() == mx.MX_OK
+    yn = y.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = int(off[g]), int(off[g + 1])
+        if hi == lo:
+            continue
+        rows = np.arange(hi - lo) if sample is None else np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64))
+        ref, ab = orc.ds_gemm(qa[lo:hi], sa[lo:hi], qb[g * N:(g + 1) * N], sb[g * N // 128:(g + 1) * N // 128], rows=rows)
+        assert_close(yn[lo + rows], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"deepseek group {g}")
+    return qa, sa, qb, sb, off, y
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_ds_grouped_half_tiles_and_empty_groups(out_dtype):
+    run_ds_grouped([128, 384, 0, 256, 128], 256, 512, out_dtype, 9900)
+
+
+def test_ds_grouped_moe_shape_sampled():
+    # the grouped-GEMM workload: 8 experts 4096 -> 14336, 16384 routed rows split unevenly
+    run_ds_grouped([3328, 1536, 2432, 1024, 2816, 1920, 2176, 1152], 14336, 4096, mx.OUT_BF16, 9910, sample=6)
+
+
+def test_ds_grouped_single_group_equals_plain_gemm():
+    M, N, K = 512, 768, 1024
+    qa, sa, qb, sb = ds_grouped_operands(M, 1, N, K, 9920)
+    args = (dev(qa), dev(sa.T), dev(qb), dev(sb))
+    y1 = mx.fp8_blockwise_gemm(*args, M, N, K, out_dtype=mx.OUT_F32)
+    y2 = mx.fp8_blockwise_gemm_grouped(*args, dev(np.array([0, M], np.int64)), M, N, K, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    assert torch.equal(y1, y2)
+
+
+def test_ds_grouped_rejects_broken_offsets_on_the_device():
+    M, N, K = 256, 256, 256
+    qa, sa, qb, sb = ds_grouped_operands(M, 2, N, K, 9930)
+    mx.fp8_blockwise_gemm_grouped(dev(qa), dev(sa.T), dev(qb), dev(sb), dev(np.array([0, 100, 256], np.int64)),
+                                  M, N, K)
+    assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
+    run_ds_grouped([128, 128], N, K, mx.OUT_BF16, 9931)
