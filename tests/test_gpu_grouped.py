@@ -328,3 +328,19 @@ def test_ds_grouped_rejects_broken_offsets_on_the_device():
                                   M, N, K)
     assert mx.mx_check() == mx.MX_ERR_INVALID_ARG
     run_ds_grouped([128, 128], N, K, mx.OUT_BF16, 9931)
+
+
+def test_nvfp4_quantize_grouped_many_groups():
+    # the most groups a call takes (1024), most of them empty, at the narrowest width (64 columns)
+    rng = np.random.default_rng(9950)
+    sizes = np.zeros(1024, np.int64)
+    sizes[rng.choice(1024, 40, replace=False)] = rng.integers(1, 4, 40) * 128
+    x = torch.cat([synthetic.normal(int(n), 64, 2.0 ** (k % 9 - 4), 9960 + k) for k, n in enumerate(sizes) if n])
+    check_nv_grouped(x.to(torch.bfloat16), [int(n) for n in sizes])
+
+
+def test_ds_grouped_many_small_groups():
+    # 64 experts of 128 or 256 rows (some empty): tiles of one group never mix with another's
+    rng = np.random.default_rng(9970)
+    sizes = (rng.integers(0, 3, 64) * 128).tolist()
+    run_ds_grouped(sizes, 256, 256, mx.OUT_F32, 9971)
