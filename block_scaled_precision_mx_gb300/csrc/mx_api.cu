@@ -30,6 +30,26 @@ mx_status launch_status() {
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
+// Every kernel is launched with programmatic stream serialization: the next kernel on the stream
+// may be scheduled while this one finishes (each kernel allows it at its start), and each kernel
+// waits for the previous one to complete before it reads memory (quantizers at their start, the
+// GEMMs after their barrier / TMEM setup).  Dependent calls stay ordered; the launch latency and
+// the GEMM setup overlap the previous kernel's last wave.
+template <typename Kern, typename... Args>
+cudaError_t pdl_launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ---------------------------------------------------------------- driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -100,7 +120,7 @@ mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const Gemm
   if (sms <= 0) return MX_ERR_CUDA;
   const int tiles = (args.M / Cfg::BM) * (args.N / BN);
   const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, args);
+  pdl_launch(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, st, ta, tb, args);
   return launch_status();
 }
 
@@ -128,7 +148,9 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -137,7 +159,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (max_clusters[dev] == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
       return MX_ERR_CUDA;
@@ -208,8 +230,8 @@ mx_status launch_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int 
                              const MxOut& o, cudaStream_t st, bool b2d = false) {
   dim3 grid;
   if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-#define MXQ(F, N, R, C) mx_quantize_kernel<F, N, R, C><<<grid, 256, 0, st>>>(x, rows, cols, o)
-#define MXQ2D(F, R, C) mx_quantize_kernel<F, 1, R, C, true><<<grid, 256, 0, st>>>(x, rows, cols, o)
+#define MXQ(F, N, R, C) pdl_launch(mx_quantize_kernel<F, N, R, C>, grid, 256, 0, st, x, rows, cols, o)
+#define MXQ2D(F, R, C) pdl_launch(mx_quantize_kernel<F, 1, R, C, true>, grid, 256, 0, st, x, rows, cols, o)
   if (b2d) {  // 2-D 32x32 blocks, MXFP8 only
     if (f0 == 0) {
       if (row && col) MXQ2D(0, true, true);
@@ -320,14 +342,14 @@ mx_status mx_quantize(const void* x, int64_t rows, int64_t cols, int block, int 
     dim3 grid;
     if (block_rows == 1) {
       if (!quant_grid(rows / 64, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-      if (pow2) ds_quantize_1x128_kernel<true><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
-      else ds_quantize_1x128_kernel<false><<<grid, 256, 0, st>>>(xb, rows, cols, qo, so);
+      if (pow2) pdl_launch(ds_quantize_1x128_kernel<true>, grid, 256, 0, st, xb, rows, cols, qo, so);
+      else pdl_launch(ds_quantize_1x128_kernel<false>, grid, 256, 0, st, xb, rows, cols, qo, so);
     } else {
       if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
       CUtensorMap tmx;  // x as bytes [rows][2 cols], boxes of 128 bytes x 128 rows
       if (!make_tmap(&tmx, x, rows, cols * 2, 128, false)) return MX_ERR_CUDA;
-      if (pow2) ds_quantize_128x128_kernel<true><<<grid, 256, 0, st>>>(tmx, rows, cols, qo, so);
-      else ds_quantize_128x128_kernel<false><<<grid, 256, 0, st>>>(tmx, rows, cols, qo, so);
+      if (pow2) pdl_launch(ds_quantize_128x128_kernel<true>, grid, 256, 0, st, tmx, rows, cols, qo, so);
+      else pdl_launch(ds_quantize_128x128_kernel<false>, grid, 256, 0, st, tmx, rows, cols, qo, so);
     }
     return launch_status();
   }
@@ -541,7 +563,7 @@ mx_status mx_scales_from_fp32_blocks(const float* s, int64_t rows, int64_t cols,
   if (!aligned(s, 4) || !aligned(s_e8m0, 16)) return MX_ERR_INVALID_ARG;
   dim3 grid;
   if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-  mx_scales_from_blocks_kernel<<<grid, 128, 0, as_stream(stream)>>>(s, rows, cols, block_rows,
+  pdl_launch(mx_scales_from_blocks_kernel, grid, 128, 0, as_stream(stream), s, rows, cols, block_rows,
                                                                       static_cast<uint8_t*>(s_e8m0));
   return launch_status();
 }
@@ -551,6 +573,7 @@ namespace {
 // nothing arrives on: the wait runs out after budget_ns, sets the abort flag and its bit in the
 // device error word, and the kernel returns.
 __global__ void selftest_wait_kernel(unsigned long long budget_ns) {
+  pdl_prologue();
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -565,7 +588,7 @@ __global__ void selftest_wait_kernel(unsigned long long budget_ns) {
 
 mx_status mx_selftest_wait_timeout(int64_t budget_us, void* stream) {
   if (budget_us < 1 || budget_us > 1000000) return MX_ERR_INVALID_ARG;
-  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(static_cast<unsigned long long>(budget_us) * 1000ull);
+  pdl_launch(selftest_wait_kernel, 1, 32, 0, as_stream(stream), static_cast<unsigned long long>(budget_us) * 1000ull);
   return launch_status();
 }
 
@@ -583,8 +606,9 @@ mx_status scale_layout(const void* src, int64_t rows, int64_t nblocks, void* dst
   if (grid > 8ll * sms) grid = 8ll * sms;
   const uint8_t* s = static_cast<const uint8_t*>(src);
   uint8_t* d = static_cast<uint8_t*>(dst);
-  if (to_plain) scale_layout_kernel<true><<<static_cast<unsigned>(grid), 256, 0, as_stream(stream)>>>(s, d, rows, nblocks);
-  else scale_layout_kernel<false><<<static_cast<unsigned>(grid), 256, 0, as_stream(stream)>>>(s, d, rows, nblocks);
+  const dim3 g(static_cast<unsigned>(grid));
+  if (to_plain) pdl_launch(scale_layout_kernel<true>, g, 256, 0, as_stream(stream), s, d, rows, nblocks);
+  else pdl_launch(scale_layout_kernel<false>, g, 256, 0, as_stream(stream), s, d, rows, nblocks);
   return launch_status();
 }
 }  // namespace
@@ -610,8 +634,8 @@ mx_status nvfp4_pass1(const uint16_t* x, int64_t rows, int64_t cols, unsigned in
   const int64_t nvec = rows * cols / 8;
   int64_t grid1 = (nvec + 255) / 256;
   if (grid1 > 8ll * sms) grid1 = 8ll * sms;
-  if (rht) nvfp4_amax_kernel<true><<<static_cast<unsigned>(grid1), 256, 0, st>>>(x, nvec, amax, signs);
-  else nvfp4_amax_kernel<false><<<static_cast<unsigned>(grid1), 256, 0, st>>>(x, nvec, amax);
+  if (rht) pdl_launch(nvfp4_amax_kernel<true>, static_cast<unsigned>(grid1), 256, 0, st, x, nvec, amax, signs);
+  else pdl_launch(nvfp4_amax_kernel<false>, static_cast<unsigned>(grid1), 256, 0, st, x, nvec, amax, 0u);
   return cudaGetLastError() == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
@@ -647,10 +671,21 @@ mx_status nvfp4_quantize_ex(const void* x, int64_t rows, int64_t cols, int use_r
   auto* q = static_cast<uint8_t*>(q_packed);
   auto* sf = static_cast<uint8_t*>(s_ue4m3);
   const auto* rb = static_cast<const uint8_t*>(rbits);
-  if (use_rht && rbits) nvfp4_quantize_kernel<true, true><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, rht_signs, rb);
-  else if (use_rht) nvfp4_quantize_kernel<true, false><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, rht_signs);
-  else if (rbits) nvfp4_quantize_kernel<false, true><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax, 0u, rb);
-  else nvfp4_quantize_kernel<false, false><<<grid, 256, 0, st>>>(xb, rows, cols, q, sf, gscale, amax);
+  // (launched through a function pointer: every parameter is passed, defaults included)
+  constexpr const uint8_t* kNoRbits = nullptr;
+  constexpr const int64_t* kNoGroups = nullptr;
+  if (use_rht && rbits)
+    pdl_launch(nvfp4_quantize_kernel<true, true>, grid, 256, 0, st, xb, rows, cols, q, sf, gscale, amax, rht_signs,
+               rb, kNoGroups, 1);
+  else if (use_rht)
+    pdl_launch(nvfp4_quantize_kernel<true, false>, grid, 256, 0, st, xb, rows, cols, q, sf, gscale, amax, rht_signs,
+               kNoRbits, kNoGroups, 1);
+  else if (rbits)
+    pdl_launch(nvfp4_quantize_kernel<false, true>, grid, 256, 0, st, xb, rows, cols, q, sf, gscale, amax, 0u, rb,
+               kNoGroups, 1);
+  else
+    pdl_launch(nvfp4_quantize_kernel<false, false>, grid, 256, 0, st, xb, rows, cols, q, sf, gscale, amax, 0u,
+               kNoRbits, kNoGroups, 1);
   return launch_status();
 }
 
@@ -668,13 +703,14 @@ mx_status nvfp4_quantize_grouped(const void* x, int64_t rows, int64_t cols, cons
   if (sms <= 0) return MX_ERR_CUDA;
   int64_t grid1 = rows / 16;
   if (grid1 > 8ll * sms) grid1 = 8ll * sms;
-  nvfp4_amax_grouped_kernel<<<static_cast<unsigned>(grid1), 256, 0, st>>>(xb, rows, cols, group_offsets, g, amax);
+  pdl_launch(nvfp4_amax_grouped_kernel, static_cast<unsigned>(grid1), 256, 0, st, xb, rows, cols, group_offsets, g,
+             amax);
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
   dim3 grid;
   if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_kernel<false, false, true><<<grid, 256, 0, st>>>(
-      xb, rows, cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3), gscale, amax, 0u, nullptr,
-      group_offsets, g);
+  pdl_launch(nvfp4_quantize_kernel<false, false, true>, grid, 256, 0, st, xb, rows, cols,
+             static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3), gscale, amax, 0u,
+             static_cast<const uint8_t*>(nullptr), group_offsets, g);
   return launch_status();
 }
 
@@ -689,7 +725,7 @@ mx_status nvfp4_quantize_2d(const void* x, int64_t rows, int64_t cols, void* q_r
   if (p1 != MX_OK) return p1;
   dim3 grid;
   if (!quant_grid(rows / 128, cols / 128, &grid)) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_2d_kernel<<<grid, 256, 0, st>>>(xb, rows, cols, static_cast<uint8_t*>(q_row),
+  pdl_launch(nvfp4_quantize_2d_kernel, grid, 256, 0, st, xb, rows, cols, static_cast<uint8_t*>(q_row),
                                                  static_cast<uint8_t*>(s_row), static_cast<uint8_t*>(q_col),
                                                  static_cast<uint8_t*>(s_col), gscale, amax);
   return launch_status();
@@ -816,6 +852,7 @@ namespace mxgb {
 // nothing in the array has to be cleared between calls.
 __global__ void __launch_bounds__(256) nvfp4_band_amax_kernel(const uint16_t* __restrict__ x, int64_t cols,
                                                               unsigned int* __restrict__ partial) {
+  pdl_prologue();
   __shared__ uint32_t wmax[8];
   const uint16_t* xb = x + static_cast<int64_t>(blockIdx.x) * kNoAllocBandRows * cols;
   const int64_t nvec = kNoAllocBandRows * cols / 8;
@@ -834,6 +871,7 @@ __global__ void __launch_bounds__(256) nvfp4_band_amax_kernel(const uint16_t* __
 // One CTA: maximum over the first `nbands` partial maxima -> *amax_out.
 __global__ void __launch_bounds__(1024) nvfp4_amax_finalize_kernel(const unsigned int* __restrict__ partial,
                                                                    int64_t nbands, unsigned int* __restrict__ amax_out) {
+  pdl_prologue();
   __shared__ uint32_t wmax[32];
   uint32_t m = 0;
   for (int64_t i = threadIdx.x; i < nbands; i += 1024) m = max(m, partial[i]);
@@ -877,15 +915,16 @@ extern "C" mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t
   if (!scratch) return MX_ERR_CUDA;
   cudaStream_t st = as_stream(stream);
   const int64_t nbands = rows / kNoAllocBandRows;
-  nvfp4_band_amax_kernel<<<static_cast<unsigned>(nbands), 256, 0, st>>>(static_cast<const uint16_t*>(x), cols,
+  pdl_launch(nvfp4_band_amax_kernel, static_cast<unsigned>(nbands), 256, 0, st, static_cast<const uint16_t*>(x), cols,
                                                                          scratch);
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
-  nvfp4_amax_finalize_kernel<<<1, 1024, 0, st>>>(scratch, nbands, scratch + kNoAllocSlots);
+  pdl_launch(nvfp4_amax_finalize_kernel, 1, 1024, 0, st, scratch, nbands, scratch + kNoAllocSlots);
   if (cudaGetLastError() != cudaSuccess) return MX_ERR_CUDA;
   dim3 grid;
   if (!quant_grid(rows / 32, (cols + 127) / 128, &grid)) return MX_ERR_INVALID_ARG;
-  nvfp4_quantize_kernel<<<grid, 256, 0, st>>>(
-      static_cast<const uint16_t*>(x), rows, cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3),
-      gscale, scratch + kNoAllocSlots);
+  pdl_launch(nvfp4_quantize_kernel<false, false, false>, grid, 256, 0, st, static_cast<const uint16_t*>(x), rows,
+             cols, static_cast<uint8_t*>(q_packed), static_cast<uint8_t*>(s_ue4m3), gscale,
+             static_cast<const unsigned int*>(scratch + kNoAllocSlots), 0u, static_cast<const uint8_t*>(nullptr),
+             static_cast<const int64_t*>(nullptr), 1);
   return launch_status();
 }

@@ -169,6 +169,7 @@ __device__ __forceinline__ uint32_t mx_cvt2(float lo, float hi) {
 template <int F0, int NF, bool ROW, bool COL, bool B2D = false>
 __global__ void __launch_bounds__(256, 4) mx_quantize_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                           int64_t cols, const MxOut o) {
+  pdl_prologue();
   __shared__ __align__(16) uint32_t tile[COL ? 128 * 64 : 1];  // 128 rows x 128 bf16 (as bf16x2 words)
   __shared__ __align__(16) uint8_t srow[NF][512];
   __shared__ __align__(16) uint8_t scol[NF][512];
@@ -400,6 +401,7 @@ __device__ __forceinline__ uint32_t e8m0_of_pow2(float sc) {
 __global__ void __launch_bounds__(128) mx_scales_from_blocks_kernel(const float* __restrict__ s, int64_t rows,
                                                                     int64_t cols, int block_rows,
                                                                     uint8_t* __restrict__ out) {
+  pdl_prologue();
   const int64_t rb = blockIdx.x, kc = blockIdx.y;
   const int i = threadIdx.x;
   const int64_t nkc = cols >> 7;
@@ -417,6 +419,7 @@ template <bool TO_PLAIN>
 __global__ void __launch_bounds__(256) scale_layout_kernel(const uint8_t* __restrict__ src,
                                                            uint8_t* __restrict__ dst, int64_t rows,
                                                            int64_t nblocks) {
+  pdl_prologue();
   const int64_t kchunks = nblocks >> 2;
   const int64_t pieces = (rows >> 7) * kchunks * 32;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < pieces;
@@ -456,6 +459,7 @@ template <bool POW2>
 __global__ void __launch_bounds__(256) ds_quantize_1x128_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                 int64_t cols, uint8_t* __restrict__ q,
                                                                 float* __restrict__ s) {
+  pdl_prologue();
   const int64_t kb = blockIdx.y;  // grid: x = group of 64 rows, y = k-block
   const int t = threadIdx.x;
   const int l4 = t & 3;
@@ -504,6 +508,7 @@ template <bool POW2>
 __global__ void __launch_bounds__(256) ds_quantize_128x128_kernel(const __grid_constant__ CUtensorMap tmx,
                                                                   int64_t rows, int64_t cols,
                                                                   uint8_t* __restrict__ q, float* __restrict__ s) {
+  pdl_prologue();
   __shared__ __align__(128) uint8_t tile[2 * 128 * 128];
   __shared__ uint64_t full;
   __shared__ uint32_t wmax[8];
@@ -635,6 +640,7 @@ __device__ __forceinline__ uint32_t nv_block_scale_code(float bamax, float sg, f
 template <bool RHT = false>
 __global__ void __launch_bounds__(256) nvfp4_amax_kernel(const uint16_t* __restrict__ x, int64_t n_vec8,
                                                          unsigned int* __restrict__ amax_bits, uint32_t signs = 0) {
+  pdl_prologue();
   __shared__ uint32_t wmax[8];
   uint32_t m = 0;  // bf16 bits (RHT: FP32 bits) of the largest magnitude
   if (RHT) {
@@ -692,6 +698,7 @@ __device__ __forceinline__ int nv_group_of(const int64_t* __restrict__ off, int 
 __global__ void __launch_bounds__(256) nvfp4_amax_grouped_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                  int64_t cols, const int64_t* __restrict__ off,
                                                                  int groups, unsigned int* __restrict__ amax) {
+  pdl_prologue();
   __shared__ uint32_t wmax[8];
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     bool good = __ldg(off) == 0 && __ldg(off + groups) == rows;
@@ -730,6 +737,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const uint16_t* __r
                                                              const unsigned int* __restrict__ amax_bits,
                                                              uint32_t signs = 0, const uint8_t* __restrict__ rbits = nullptr,
                                                              const int64_t* __restrict__ off = nullptr, int groups = 1) {
+  pdl_prologue();
   // grid: x = 32-row tile, y = 128-column tile; the last column tile may be half full
   // (cols % 128 == 64)
   __shared__ float s_glob[2];  // s_g and rcp(s_g), computed once per CTA
@@ -821,6 +829,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_2d_kernel(const uint16_t* 
                                                                 uint8_t* __restrict__ q_col,
                                                                 uint8_t* __restrict__ s_col, float* __restrict__ gscale,
                                                                 const unsigned int* __restrict__ amax_bits) {
+  pdl_prologue();
   __shared__ __align__(16) uint32_t ctile[128 * 16];  // 128 rows x 128 packed codes
   __shared__ __align__(16) uint8_t srow[1024], scol[1024];
   __shared__ uint32_t bmax[64];

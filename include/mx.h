@@ -5,7 +5,10 @@
  * Conventions shared by every entry point
  *  - All tensor pointers are CALLER-OWNED DEVICE memory.  No call allocates or frees.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
- *    legacy default stream).  No call synchronizes the host.
+ *    legacy default stream).  No call synchronizes the host.  Kernels are launched with
+ *    programmatic dependent launch: one may be scheduled while the previous kernel on the
+ *    stream finishes, but it reads no memory before that kernel has completed, so stream
+ *    order holds for every input, whichever kernel wrote it.
  *  - Matrices are row-major.  A GEMM computes C[m][n] = sum_k A[m][k] * B[n][k]: both code
  *    operands are K-contiguous ("TN" in column-major BLAS terms).  Column-wise quantized
  *    copies are stored physically transposed, so fprop, dgrad and wgrad all run as this one
