@@ -59,6 +59,48 @@ __device__ __forceinline__ void store_chunk_32x32(const CUtensorMap* tmOut, uint
   }
 }
 
+// Grouped products: per-group first tile numbers (tiles numbered group by group, each group's
+// rows in BM-row tiles times num_nb column tiles).  Offsets must start at 0, end at M, be
+// multiples of 128 and never decrease; otherwise every entry is 0 (no tile runs) and the error
+// word reports it.  One thread fills the table; the caller synchronizes before others read it.
+__device__ __forceinline__ void build_group_table(int* grp_start, const GemmArgs& args, int bm, int num_nb) {
+  const int64_t* off = args.group_off;
+  bool good = __ldg(off) == 0 && __ldg(off + args.groups) == args.M;
+  int t = 0;
+  for (int g = 0; g < args.groups; ++g) {
+    grp_start[g] = t;
+    const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
+    good = good && a >= 0 && b >= a && (a & 127) == 0 && (b & 127) == 0 && b <= args.M;
+    if (good) t += static_cast<int>((b - a + bm - 1) / bm) * num_nb;
+  }
+  if (!good) {
+    t = 0;
+    if (blockIdx.x == 0) atomicOr(&g_mx_error_word, kSiteBadGroups);
+  }
+  grp_start[args.groups] = t;
+}
+
+// Grouped tile -> group, first A row of the tile, first row of B (the experts' blocks stacked),
+// rows of the group from a_row0 on (at most bm), column tile.
+__device__ __forceinline__ void decode_group_tile(const int* grp_start, const GemmArgs& args, int bm, int bn,
+                                                  int num_nb, int tile, int& grp, int64_t& a_row0, int64_t& b_row0,
+                                                  int& rows_valid, int& nb) {
+  int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (grp_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int64_t off = __ldg(args.group_off + lo), rows_g = __ldg(args.group_off + lo + 1) - off;
+  int mb;
+  tile_coords(tile - grp_start[lo], static_cast<int>((rows_g + bm - 1) / bm), num_nb, mb, nb);
+  a_row0 = off + static_cast<int64_t>(mb) * bm;
+  b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * bn;
+  const int64_t left = rows_g - static_cast<int64_t>(mb) * bm;
+  rows_valid = left < bm ? static_cast<int>(left) : bm;
+  grp = lo;
+}
+
 // byte offset of row i's 4 scale bytes inside a 512-byte MX scale chunk
 __device__ __forceinline__ int chunk_offset_mx(int i) { return (i & 31) * 16 + (i >> 5) * 4; }
 
@@ -160,24 +202,7 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
   const int num_nb = args.N / Cfg::BN;
   const int num_kt = args.K / Cfg::K_ELEMS;
   __shared__ int grp_start[GROUPED ? kMaxGroups + 1 : 1];  // first tile of each group
-  if (GROUPED && threadIdx.x == 0) {
-    // offsets must start at 0, end at M, be multiples of 128 and never decrease; otherwise no
-    // tile runs and the error word reports it
-    const int64_t* off = args.group_off;
-    bool good = __ldg(off) == 0 && __ldg(off + args.groups) == args.M;
-    int t = 0;
-    for (int g = 0; g < args.groups; ++g) {
-      grp_start[g] = t;
-      const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
-      good = good && a >= 0 && b >= a && (a & 127) == 0 && (b & 127) == 0 && b <= args.M;
-      if (good) t += static_cast<int>((b - a + Cfg::BM - 1) / Cfg::BM) * num_nb;
-    }
-    if (!good) {
-      t = 0;
-      if (blockIdx.x == 0) atomicOr(&g_mx_error_word, kSiteBadGroups);
-    }
-    grp_start[args.groups] = t;
-  }
+  if (GROUPED && threadIdx.x == 0) build_group_table(grp_start, args, Cfg::BM, num_nb);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -209,23 +234,11 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
   const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
   // tile -> (first A row, first B row, rows of A that belong to it, output column block)
   auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb, int& grp) {
-    int mb;
     grp = 0;
     if (GROUPED) {
-      int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (grp_start[mid] <= tile) lo = mid;
-        else hi = mid - 1;
-      }
-      const int64_t off = __ldg(args.group_off + lo), rows_g = __ldg(args.group_off + lo + 1) - off;
-      tile_coords(tile - grp_start[lo], static_cast<int>((rows_g + Cfg::BM - 1) / Cfg::BM), num_nb, mb, nb);
-      a_row0 = off + static_cast<int64_t>(mb) * Cfg::BM;
-      b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * Cfg::BN;
-      const int64_t left = rows_g - static_cast<int64_t>(mb) * Cfg::BM;
-      rows_valid = left < Cfg::BM ? static_cast<int>(left) : Cfg::BM;
-      grp = lo;
+      decode_group_tile(grp_start, args, Cfg::BM, Cfg::BN, num_nb, tile, grp, a_row0, b_row0, rows_valid, nb);
     } else {
+      int mb;
       tile_coords(tile, num_mb, num_nb, mb, nb);
       a_row0 = static_cast<int64_t>(mb) * Cfg::BM;
       b_row0 = static_cast<int64_t>(nb) * Cfg::BN;
@@ -596,42 +609,15 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16, GROUPED>::THREADS, 1)
   const int num_nb = args.N / Cfg::BN;
   const int num_kt = args.K / 128;
   __shared__ int grp_start[GROUPED ? kMaxGroups + 1 : 1];  // first tile of each group
-  if (GROUPED && threadIdx.x == 0) {
-    // offsets must start at 0, end at M, be multiples of 128 and never decrease; otherwise no
-    // tile runs and the error word reports it
-    const int64_t* off = args.group_off;
-    bool good = __ldg(off) == 0 && __ldg(off + args.groups) == args.M;
-    int t = 0;
-    for (int g = 0; g < args.groups; ++g) {
-      grp_start[g] = t;
-      const int64_t a = __ldg(off + g), b = __ldg(off + g + 1);
-      good = good && a >= 0 && b >= a && (a & 127) == 0 && (b & 127) == 0 && b <= args.M;
-      if (good) t += static_cast<int>((b - a + Cfg::BM - 1) / Cfg::BM) * num_nb;
-    }
-    if (!good) {
-      t = 0;
-      if (blockIdx.x == 0) atomicOr(&g_mx_error_word, kSiteBadGroups);
-    }
-    grp_start[args.groups] = t;
-  }
+  if (GROUPED && threadIdx.x == 0) build_group_table(grp_start, args, Cfg::BM, num_nb);
   // tile -> first A row of the pair, first B row (of the stacked experts), rows of the group from
   // a_row0 on, n-block
   auto decode = [&](int tile, int64_t& a_row0, int64_t& b_row0, int& rows_valid, int& nb) {
-    int mb;
     if (GROUPED) {
-      int lo = 0, hi = args.groups - 1;  // the last group whose first tile is <= tile
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (grp_start[mid] <= tile) lo = mid;
-        else hi = mid - 1;
-      }
-      const int64_t off = __ldg(args.group_off + lo), rows_g = __ldg(args.group_off + lo + 1) - off;
-      tile_coords(tile - grp_start[lo], static_cast<int>((rows_g + Cfg::BM - 1) / Cfg::BM), num_nb, mb, nb);
-      a_row0 = off + static_cast<int64_t>(mb) * Cfg::BM;
-      b_row0 = static_cast<int64_t>(lo) * args.N + static_cast<int64_t>(nb) * Cfg::BN;
-      const int64_t left = rows_g - static_cast<int64_t>(mb) * Cfg::BM;
-      rows_valid = left < Cfg::BM ? static_cast<int>(left) : Cfg::BM;
+      int grp;
+      decode_group_tile(grp_start, args, Cfg::BM, Cfg::BN, num_nb, tile, grp, a_row0, b_row0, rows_valid, nb);
     } else {
+      int mb;
       tile_coords(tile, num_mb, num_nb, mb, nb);
       a_row0 = static_cast<int64_t>(mb) * Cfg::BM;
       b_row0 = static_cast<int64_t>(nb) * Cfg::BN;
