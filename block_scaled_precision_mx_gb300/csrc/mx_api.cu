@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -82,22 +83,24 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_byt
 }
 
 // ---------------------------------------------------------------- device properties
+// Per-device caches, filled on first use; atomics so that host threads calling concurrently
+// read and write them without a data race (they all compute the same values).
 struct DevInfo {
-  int sms = 0;
+  std::atomic<int> sms{0};
 };
 DevInfo g_dev[64];
-int g_last_sms = 0;
+std::atomic<int> g_last_sms{0};
 
 int device_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (g_dev[dev].sms == 0) {
-    int n = 0;
+  int n = g_dev[dev].sms.load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    g_dev[dev].sms = n;
+    g_dev[dev].sms.store(n, std::memory_order_relaxed);
   }
-  g_last_sms = g_dev[dev].sms;
-  return g_dev[dev].sms;
+  g_last_sms.store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // ---------------------------------------------------------------- GEMM launch
@@ -105,13 +108,13 @@ template <int KIND, int BN, bool OUT_BF16>
 mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st) {
   using Cfg = GemmCfg<KIND, BN>;
   auto kern = bs_gemm_kernel<KIND, BN, OUT_BF16>;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
+  if (!attr_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
       return MX_ERR_CUDA;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_relaxed);
   }
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, qa, args.M, kbytes, Cfg::BM)) return MX_ERR_CUDA;
@@ -143,7 +146,8 @@ bool make_out_tmap(CUtensorMap* map, void* out, int64_t M, int64_t N, int64_t ld
 // (each persistent over its share of `tiles`).  `max_clusters` caches the occupancy per device
 // for this kernel.
 template <typename... KArgs, typename... Args>
-mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int tiles, int (&max_clusters)[64],
+mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int tiles,
+                       std::atomic<int> (&max_clusters)[64],
                        cudaStream_t st, Args... args) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
@@ -160,16 +164,16 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (max_clusters[dev] == 0) {
+  int n = max_clusters[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
       return MX_ERR_CUDA;
     const int sms = device_sms();
     cfg.gridDim = dim3(static_cast<unsigned>(sms - (sms & 1)));
-    int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return MX_ERR_CUDA;
-    max_clusters[dev] = n;
+    max_clusters[dev].store(n, std::memory_order_relaxed);
   }
-  const int clusters = tiles < max_clusters[dev] ? tiles : max_clusters[dev];
+  const int clusters = tiles < n ? tiles : n;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
   if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return MX_ERR_CUDA;
   return launch_status();
@@ -180,7 +184,7 @@ template <int KIND, bool OUT_BF16, bool GROUPED = false, int MXOUT = -1>
 mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const GemmArgs& args, cudaStream_t st,
                        int64_t b_rows = 0) {
   using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUPED>;
-  static int max_clusters[64] = {};
+  static std::atomic<int> max_clusters[64];
   const int64_t kc = (KIND == kNvf4) ? args.K / 64 : args.K / 128;  // 512-byte scale chunks per 128 rows
   const int chunk_rows = Cfg::SF_CHUNK / 128;
   CUtensorMap ta, tb, tsa, tsb, tout;
@@ -206,7 +210,7 @@ mx_status launch_gemm2(const void* qa, const void* qb, int64_t kbytes, const Gem
 template <bool OUT_BF16, bool GROUPED = false>
 mx_status launch_ds_gemm2(const void* qa, const void* qb, const GemmArgs& args, cudaStream_t st, int64_t b_rows = 0) {
   using Cfg = Ds2Cfg<OUT_BF16, GROUPED>;
-  static int max_clusters[64] = {};
+  static std::atomic<int> max_clusters[64];
   CUtensorMap ta, tb, tout;
   if (!make_tmap(&ta, qa, args.M, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
   if (!make_tmap(&tb, qb, GROUPED ? b_rows : args.N, args.K, Cfg::ROWS)) return MX_ERR_CUDA;
@@ -290,7 +294,7 @@ const char* mx_status_string(mx_status s) {
   return "MX_ERR_UNKNOWN";
 }
 
-int mx_num_sms(void) { return g_last_sms; }
+int mx_num_sms(void) { return g_last_sms.load(std::memory_order_relaxed); }
 
 size_t mx_scale_bytes(int64_t rows, int64_t cols, int block, int block_rows, mx_scale_fmt sfmt) {
   if (rows <= 0 || cols <= 0) return 0;
@@ -413,7 +417,9 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
       return bf ? launch_gemm2<kMxf4, true>(qa, qb, kb, a, st) : launch_gemm2<kMxf4, false>(qa, qb, kb, a, st);
     }
     a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 1);
-    if (bn256) return bf ? launch_gemm<kMxf4, 256, true>(qa, qb, kb, a, st) : launch_gemm<kMxf4, 256, false>(qa, qb, kb, a, st);
+    if (bn256)
+      return bf ? launch_gemm<kMxf4, 256, true>(qa, qb, kb, a, st)
+                : launch_gemm<kMxf4, 256, false>(qa, qb, kb, a, st);
     return bf ? launch_gemm<kMxf4, 128, true>(qa, qb, kb, a, st) : launch_gemm<kMxf4, 128, false>(qa, qb, kb, a, st);
   }
   if (bn256 && (M % 256) == 0) {
@@ -421,7 +427,9 @@ mx_status mx_gemm(const void* qa, const void* sa, mx_elem ea, const void* qb, co
     return bf ? launch_gemm2<kMxf8, true>(qa, qb, K, a, st) : launch_gemm2<kMxf8, false>(qa, qb, K, a, st);
   }
   a.idesc = make_idesc_block_scaled(static_cast<uint32_t>(ea), static_cast<uint32_t>(eb), 128, bn256 ? 256 : 128, 1);
-  if (bn256) return bf ? launch_gemm<kMxf8, 256, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 256, false>(qa, qb, K, a, st);
+  if (bn256)
+    return bf ? launch_gemm<kMxf8, 256, true>(qa, qb, K, a, st)
+              : launch_gemm<kMxf8, 256, false>(qa, qb, K, a, st);
   return bf ? launch_gemm<kMxf8, 128, true>(qa, qb, K, a, st) : launch_gemm<kMxf8, 128, false>(qa, qb, K, a, st);
 }
 
@@ -757,7 +765,9 @@ mx_status nvfp4_gemm(const void* qa, const void* sa, const float* ga, const void
     return bf ? launch_gemm2<kNvf4, true>(qa, qb, kb, a, st) : launch_gemm2<kNvf4, false>(qa, qb, kb, a, st);
   }
   a.idesc = make_idesc_block_scaled(1u, 1u, 128, bn256 ? 256 : 128, 0);
-  if (bn256) return bf ? launch_gemm<kNvf4, 256, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 256, false>(qa, qb, kb, a, st);
+  if (bn256)
+    return bf ? launch_gemm<kNvf4, 256, true>(qa, qb, kb, a, st)
+              : launch_gemm<kNvf4, 256, false>(qa, qb, kb, a, st);
   return bf ? launch_gemm<kNvf4, 128, true>(qa, qb, kb, a, st) : launch_gemm<kNvf4, 128, false>(qa, qb, kb, a, st);
 }
 
