@@ -636,7 +636,7 @@ namespace {
 // transformed values when rht).
 mx_status nvfp4_pass1(const uint16_t* x, int64_t rows, int64_t cols, unsigned int* amax, bool rht, uint32_t signs,
                       cudaStream_t st) {
-  if (cudaMemsetAsync(amax, 0, sizeof(unsigned int), st) != cudaSuccess) return MX_ERR_CUDA;
+  if (pdl_launch(zero_words_kernel, 1, 256, 0, st, amax, 1) != cudaSuccess) return MX_ERR_CUDA;
   const int sms = device_sms();
   if (sms <= 0) return MX_ERR_CUDA;
   const int64_t nvec = rows * cols / 8;
@@ -706,7 +706,7 @@ mx_status nvfp4_quantize_grouped(const void* x, int64_t rows, int64_t cols, cons
   auto* amax = static_cast<unsigned int*>(workspace);
   const auto* xb = static_cast<const uint16_t*>(x);
   const int g = static_cast<int>(groups);
-  if (cudaMemsetAsync(amax, 0, sizeof(unsigned int) * static_cast<size_t>(g), st) != cudaSuccess) return MX_ERR_CUDA;
+  if (pdl_launch(zero_words_kernel, (g + 255) / 256, 256, 0, st, amax, g) != cudaSuccess) return MX_ERR_CUDA;
   const int sms = device_sms();
   if (sms <= 0) return MX_ERR_CUDA;
   int64_t grid1 = rows / 16;

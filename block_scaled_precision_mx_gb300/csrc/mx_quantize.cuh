@@ -677,6 +677,13 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
+// Clears n words (the NVFP4 amax workspace) as a kernel of the stream's dependent-launch chain,
+// after the previous kernel (which may still read them) has completed.
+__global__ void __launch_bounds__(256) zero_words_kernel(unsigned int* __restrict__ p, int n) {
+  pdl_prologue();
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) p[i] = 0u;
+}
+
 // Grouped NVFP4 (row groups of one matrix quantized as tensors of their own, e.g. the weights of
 // MoE experts; "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 5.4 applied per group).
 // The group of row r: the last g < G with off[g] <= r.  Always in [0, G), whatever off holds, so
