@@ -31,11 +31,14 @@ mx_status launch_status() {
   return e == cudaSuccess ? MX_OK : MX_ERR_CUDA;
 }
 
-// Every kernel is launched with programmatic stream serialization: the next kernel on the stream
-// may be scheduled while this one finishes (each kernel allows it at its start), and each kernel
-// waits for the previous one to complete before it reads memory (quantizers at their start, the
-// GEMMs after their barrier / TMEM setup).  Dependent calls stay ordered; the launch latency and
-// the GEMM setup overlap the previous kernel's last wave.
+// The quantizers and small helper kernels are launched with programmatic stream serialization:
+// one may be scheduled while the previous kernel on the stream finishes (each allows it at its
+// start) and waits for that kernel to complete before it reads memory, so dependent calls stay
+// ordered and the launch latency overlaps the previous kernel's last wave.  The GEMMs take no
+// part: they are launched the ordinary way and do not let the next kernel start early.  Their
+// persistent CTAs take tiles in a fixed order; early-started CTAs on the SMs a previous kernel
+// left first, or a next kernel's CTAs waiting on SMs the GEMM left first, made a full step 3-5%
+// slower in both cases.
 template <typename Kern, typename... Args>
 cudaError_t pdl_launch(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
@@ -123,7 +126,7 @@ mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const Gemm
   if (sms <= 0) return MX_ERR_CUDA;
   const int tiles = (args.M / Cfg::BM) * (args.N / BN);
   const int grid = tiles < sms ? tiles : sms;
-  pdl_launch(kern, grid, Cfg::THREADS, Cfg::SMEM_BYTES, st, ta, tb, args);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(ta, tb, args);  // not a dependent launch (see above)
   return launch_status();
 }
 
@@ -152,9 +155,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MX_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -163,7 +164,7 @@ mx_status launch_pairs(void (*kern)(KArgs...), int threads, int smem_bytes, int 
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   int n = max_clusters[dev].load(std::memory_order_relaxed);
   if (n == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)

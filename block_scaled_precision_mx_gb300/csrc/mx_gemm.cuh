@@ -144,8 +144,6 @@ template <int KIND, int BN, bool OUT_BF16>
 __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs args) {
-  pdl_trigger();
-
   using Cfg = GemmCfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -194,7 +192,6 @@ __global__ void __launch_bounds__(GemmCfg<KIND, BN>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  pdl_wait();  // the prologue overlapped the previous kernel
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 

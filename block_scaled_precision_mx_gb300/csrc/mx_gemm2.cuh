@@ -170,8 +170,6 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
     bs_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                     const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
-  pdl_trigger();
-  if (GROUPED) pdl_wait();  // the group table below reads the offsets
   using Cfg = Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUPED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -228,7 +226,6 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
   }
   tc_fence_before();
   cluster_sync_all();
-  if (!GROUPED) pdl_wait();  // the prologue overlapped the previous kernel
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
@@ -582,8 +579,6 @@ template <bool OUT_BF16, bool GROUPED = false>
 __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16, GROUPED>::THREADS, 1)
     ds_gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmOut, const GemmArgs args) {
-  pdl_trigger();
-  if (GROUPED) pdl_wait();
   using Cfg = Ds2Cfg<OUT_BF16, GROUPED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -647,7 +642,6 @@ __global__ void __launch_bounds__(Ds2Cfg<OUT_BF16, GROUPED>::THREADS, 1)
   }
   tc_fence_before();
   cluster_sync_all();
-  if (!GROUPED) pdl_wait();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = GROUPED ? grp_start[args.groups] : num_mb * num_nb;
