@@ -221,7 +221,7 @@ class Workload:
             self.A4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
             self.B4q = (u8(8192, 4096), u8(sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)), f32(1), u8(16))
             self.Y4 = f32(8192, 8192)
-            self.launches_per_step += 5
+            self.launches_per_step += 7
             self._outs += [self.Y4]
         if "ds" in groups:
             self.A5q = (u8(4096, 7168), f32(56, 4096))
@@ -253,7 +253,7 @@ class Workload:
             # DeepSeek FP8 experts: tokens in 1x128 tiles, the stacked weights in 128x128 blocks
             self.A9d = (u8(m9, 4096), f32(4096 // 128, m9))
             self.B9d = (u8(n9, 4096), f32(n9 // 128, 4096 // 128))
-            self.launches_per_step += 5
+            self.launches_per_step += 6
             self._outs += [self.Y9]
         if "nvt" in groups:
             g8 = torch.Generator(device="cpu").manual_seed(8100)
@@ -261,7 +261,7 @@ class Workload:
             nsb = sb(8192, 8192, 16, 1, mx.SCALE_UE4M3)
             self.A8q = (u8(8192, 4096), u8(nsb), f32(1), u8(16))
             self.A8t = (u8(8192, 4096), u8(nsb), u8(4096, 8192), u8(nsb))
-            self.launches_per_step += 8
+            self.launches_per_step += 12
             self._outs += [self.A8q[0], self.A8t[0], self.A8t[2]]
         if "blk" in groups:
             self.A7q = (u8(4096, 7168), f32(56, 4096), u8(4096 * 7168 // 32))
@@ -698,10 +698,10 @@ def main():
     kernels = {k: [r for r in v if r in present] for k, v in kernels.items()}
     kernels = {k: v for k, v in kernels.items() if v}
     launches = {"mx_gemm": len(kernels.get("mx_gemm", [])), "nvfp4_gemm": 1, "fp8_blockwise_gemm": 1,
-                "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 4,
+                "mx_quantize": 1 * ("q2" in present) + 3 * ("linq" in present), "nvfp4_quantize": 6,
                 "ds_quantize": 2, "mxfp4_gemm": 1, "mxfp4_quantize": 2, "mx_gemm_blocks": 1,
                 "pow2_block_quantize": 2, "mx_scales_from_fp32_blocks": 2, "mx_quantize_2d32": 1,
-                "nvfp4_quantize_ex": 6, "nvfp4_quantize_2d": 2, "nvfp4_quantize_grouped": 2, "mx_gemm_grouped": 1,
+                "nvfp4_quantize_ex": 9, "nvfp4_quantize_2d": 3, "nvfp4_quantize_grouped": 3, "mx_gemm_grouped": 1,
                 "nvfp4_gemm_grouped": 1, "fp8_blockwise_gemm_grouped": 1, "mx_gemm_mxout": 2,
                 "mx_gemm_then_quantize": 2}
     dom = max(kernels, key=lambda k: sum(rows_ms[r] for r in kernels[k]))
