@@ -101,6 +101,25 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# Dense tensor-core peaks.  "NVFP4: high accuracy with 4 bits" (theluyuan.com), sec 8, gives the
+# dense rates as FP4 : FP8 : BF16 = 9 : 4.5 : 2.25 PFLOP/s, i.e. FP8 = 2x and FP4 = 4x BF16.  The
+# FP8 and FP4 peaks are derived from the measured BF16 rate by that ratio; the BF16 figure is the
+# burst one (a cuBLAS GEMM timed alone), because every timed GEMM here is one launch of a few
+# hundred microseconds inside a sub-second region, not a seconds-long loop under the power cap
+# (that loop ran at a median 1462 MHz; the bench's GEMMs run near 2000 MHz).
+NOMINAL_TFLOPS = {"fp8": 4500.0, "fp4": 9000.0}
+FP4_ROWS = ("nvgemm", "mx4gemm", "moe4gemm")
+
+
+def tensor_peaks(peaks):
+    """Derived dense peaks (TFLOP/s) for FP8 and FP4 from the measured BF16 burst rate."""
+    b = peaks["bf16_tflops"]
+    return {"fp8": 2.0 * b, "fp4": 4.0 * b,
+            "source": f"{peaks['source']} bf16 burst {b:g} TFLOP/s x 2 (FP8) / x 4 (FP4): dense ratio "
+                      "FP4:FP8:BF16 = 9:4.5:2.25 ('NVFP4: high accuracy with 4 bits' sec 8); nominal "
+                      "FP8 4500 / FP4 9000 TFLOP/s beside it"}
+
+
 # ------------------------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -158,46 +177,134 @@ class ClockSampler:
                 "samples": len(mhz)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's libnvidia-ml, by ctypes)
+    every couple of milliseconds, so that a timed region of a few tens of milliseconds still gets
+    dozens of samples.  Reads only; falls back to ClockSampler (nvidia-smi) where NVML cannot be
+    loaded."""
+    NVML_CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid, index, period_s=0.002):
+        self.uuid, self.index, self.period = uuid, index, period_s
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self.thread = None
+
+    def start(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = 1
+            if self.uuid:
+                rc = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(self.index)), ctypes.byref(h))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint(0)
+            lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except (OSError, AttributeError, ValueError):
+            return
+        self.ok = True
+
+        def run():
+            mhz, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self._stop.is_set():
+                if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) == 0 and \
+                        reasons_fn(h, ctypes.byref(rs)) == 0:
+                    self.samples.append((time.time(), float(mhz.value), int(rs.value)))
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [r for r in self.samples if t0 <= r[0] <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": getattr(self, "max_mhz", None), "reasons": [], "samples": 0,
+                    "source": "nvml"}
+        reasons = sorted({name for (_, _, bits) in rows for b, name in self.REASONS.items() if bits & b})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(rows), "sm_mhz_min": min(r[1] for r in rows), "source": "nvml"}
+
+
+def clock_sampler(dev_index):
+    """An NVML sampler for the GPU torch calls `dev_index`, else nvidia-smi's."""
+    import torch
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev_index)).split(",")[dev_index] if os.environ.get(
+        "CUDA_VISIBLE_DEVICES") else str(dev_index)
+    uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except (AttributeError, RuntimeError):
+        uuid = phys if phys.startswith("GPU-") else None
+    s = NvmlSampler(uuid, phys if phys.isdigit() else dev_index)
+    s.start()
+    if s.ok:
+        return s
+    s = ClockSampler(phys)
+    s.start()
+    return s
+
+
 # ------------------------------------------------------------------------------------ workload
+def make_host_inputs(groups):
+    """The seeded bf16 inputs of the given row groups, on the host (CPU tensors)."""
+    from block_scaled_precision_mx_gb300 import synthetic
+    host = {}
+    if "q2" in groups:
+        host["x2"] = synthetic.mxfp8_quantize()
+    if "lin" in groups:
+        host["X"], host["W"], host["G"] = synthetic.mxfp8_linear()
+    if "nv" in groups:
+        host["A4"], host["B4"] = synthetic.nvfp4_pair()
+    if "ds" in groups:
+        host["A5"], host["B5"] = synthetic.deepseek_pair()
+    if "mx4" in groups:
+        host["A6"], host["B6"] = synthetic.mxfp4_pair()
+    if "nvt" in groups:
+        host["A8"] = synthetic.nvfp4_pair()[0]
+    if "fuse" in groups:
+        host["X10"], host["W10"], _ = synthetic.mxfp8_linear()
+    if "moe" in groups:
+        host["A9"] = synthetic.normal(sum(MOE_SIZES), 4096, 1.0, 9000)
+        host["B9"] = synthetic.normal(len(MOE_SIZES) * 14336, 4096, 0.02, 9001)
+    if "blk" in groups:
+        host["A7"], host["B7"] = synthetic.deepseek_pair()
+        host["W7"] = synthetic.mxfp8_linear()[1]
+    return host
+
+
 class Workload:
     """All inputs and outputs of one step, resident on the device."""
 
     GROUPS = ("q2", "lin", "nv", "ds")   # the default step; "mx4" only with --only
 
     def __init__(self, dev, groups=GROUPS, host=None):
-        """host: the host inputs of another Workload to reuse (a second buffer set for the
-        pipelined end-to-end run) instead of drawing them again."""
+        """host: host inputs to reuse (from make_host_inputs, or another Workload's for the second
+        buffer set of the pipelined end-to-end run) instead of drawing them again."""
         import torch
-        from block_scaled_precision_mx_gb300 import synthetic
         import block_scaled_precision_mx_gb300 as mx
         self.mx = mx
         self.torch = torch
         self.dev = dev
         self.groups = tuple(groups)
         t = lambda x: x.to(dev)
-        self.host = {} if host is None else dict(host)
-        if host is not None:
-            groups = ()  # inputs given; only the device buffers below are made
-        if "q2" in groups:
-            self.host["x2"] = synthetic.mxfp8_quantize()
-        if "lin" in groups:
-            self.host["X"], self.host["W"], self.host["G"] = synthetic.mxfp8_linear()
-        if "nv" in groups:
-            self.host["A4"], self.host["B4"] = synthetic.nvfp4_pair()
-        if "ds" in groups:
-            self.host["A5"], self.host["B5"] = synthetic.deepseek_pair()
-        if "mx4" in groups:
-            self.host["A6"], self.host["B6"] = synthetic.mxfp4_pair()
-        if "nvt" in groups:
-            self.host["A8"] = synthetic.nvfp4_pair()[0]
-        if "fuse" in groups:
-            self.host["X10"], self.host["W10"], _ = synthetic.mxfp8_linear()
-        if "moe" in groups:
-            self.host["A9"] = synthetic.normal(sum(MOE_SIZES), 4096, 1.0, 9000)
-            self.host["B9"] = synthetic.normal(len(MOE_SIZES) * 14336, 4096, 0.02, 9001)
-        if "blk" in groups:
-            self.host["A7"], self.host["B7"] = synthetic.deepseek_pair()
-            self.host["W7"] = synthetic.mxfp8_linear()[1]
+        self.host = make_host_inputs(groups) if host is None else dict(host)
         self.d = {k: t(v) for k, v in self.host.items()}
         groups = self.groups
         u8 = lambda *s: torch.empty(*s, dtype=torch.uint8, device=dev)
@@ -401,8 +508,6 @@ ROW_ORDER = ["q2", "linq", "fprop", "dgrad", "wgrad", "nvq", "nvgemm", "dsq", "d
 def row_report(name, ms, peaks):
     """Per-row throughput and roofline fraction from its average time per step (ms)."""
     s = ms / 1e3
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]      # FP8 dense = 2x BF16 (4.5 / 2.25 nominal)
-    fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]      # FP4 dense = 6x BF16 (13.5 / 2.25 nominal)
     hbm_rows = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES, "mx4q": MX4Q_BYTES,
                 "blkq": DSQ_BYTES, "blkconv": BLKCONV_BYTES, "w2dq": W2DQ_BYTES, "nvq_rht": NVT_RHT_BYTES,
                 "nvq_sr": NVT_SR_BYTES, "nvq_rht_sr": NVT_SR_BYTES, "nvq_2d": NVT_2D_BYTES, "moe4q": MOE4Q_BYTES}
@@ -411,72 +516,102 @@ def row_report(name, ms, peaks):
         gbs = b / s / 1e9
         return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "bound": "hbm", "bytes": int(b)}
-    f = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-         "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "moedsgemm": F_MOE, "fusedgemm": F_LIN,
-         "fusedboth": F_LIN, "unfused": F_LIN}[name]
+    f = ROW_FLOPS[name]
     tf = f / s / 1e12
-    peak = fp4_peak if name in ("nvgemm", "mx4gemm", "moe4gemm") else fp8_peak
-    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4), "bound": "tensor",
-            "flops": int(f)}
+    kind = "fp4" if name in FP4_ROWS else "fp8"
+    peak = tensor_peaks(peaks)[kind]
+    return {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4),
+            "frac_nominal": round(tf / NOMINAL_TFLOPS[kind], 4), "bound": "tensor", "peak": kind, "flops": int(f)}
+
+
+ROW_FLOPS = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
+             "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "moedsgemm": F_MOE, "fusedgemm": F_LIN,
+             "fusedboth": F_LIN, "unfused": F_LIN}
 
 
 # ------------------------------------------------------------------------------------ CPU oracle
-def oracle_sample_run():
-    """Time the CPU oracle on a bounded sample of one step; returns (projected step seconds,
-    description, threads)."""
+ORACLE_GEMMS = ("fprop", "dgrad", "wgrad", "nvgemm", "dsgemm")
+ORACLE_QUANT_BYTES = {"q2": Q2_BYTES, "linq": LINQ_BYTES, "nvq": NVQ_BYTES, "dsq": DSQ_BYTES}
+
+
+def oracle_quantize_all(host):
+    """Every quantizer of the default step on its full tensor, by the CPU oracle.  Returns the
+    oracle's codes and scales the sampled products read, and the seconds each row took."""
+    import oracle as orc
+    t, out = {}, {}
+
+    def timed(name, fn):
+        t0 = time.perf_counter()
+        r = fn()
+        t[name] = time.perf_counter() - t0
+        return r
+
+    timed("q2", lambda: [(orc.mx_quantize_rowwise(host["x2"], f), orc.mx_quantize_colwise(host["x2"], f))
+                         for f in (orc.E4M3, orc.E5M2)])
+
+    def linq():
+        for name, f in (("X", orc.E4M3), ("W", orc.E4M3), ("G", orc.E5M2)):
+            out[name] = (orc.mx_quantize_rowwise(host[name], f), orc.mx_quantize_colwise(host[name], f))
+    timed("linq", linq)
+    out["A4"], out["B4"] = timed("nvq", lambda: (orc.nv_quantize(host["A4"]), orc.nv_quantize(host["B4"])))
+    out["A5"], out["B5"] = timed("dsq", lambda: (orc.ds_quantize_1x128(host["A5"]), orc.ds_quantize_128x128(host["B5"])))
+    return out, t
+
+
+def oracle_gemm_sample(q, rows_per_gemm, which=ORACLE_GEMMS):
+    """The products `which` of the default step, each on `rows_per_gemm` evenly spaced output rows
+    (all N columns, full K), from the oracle's own codes; returns {row: (seconds, flops,
+    full-size flops)}."""
     import numpy as np
     import oracle as orc
-    from block_scaled_precision_mx_gb300 import synthetic
-    orc.build()
-    t_total = 0.0
-    parts = []
-
-    def timed(fn, scale, what):
-        nonlocal t_total
+    (xr, xc), (wr, wc), (gr, gc) = q["X"], q["W"], q["G"]
+    prods = {  # name: (fn(rows), M, N, K)
+        "fprop": (lambda r: orc.mx_gemm(xr[0], xr[1], orc.E4M3, wr[0], wr[1], orc.E4M3, rows=r), 8192, 14336, 4096),
+        "dgrad": (lambda r: orc.mx_gemm(gr[0], gr[1], orc.E5M2, wc[0], wc[1], orc.E4M3, rows=r), 8192, 4096, 14336),
+        "wgrad": (lambda r: orc.mx_gemm(gc[0], gc[1], orc.E5M2, xc[0], xc[1], orc.E4M3, rows=r), 14336, 4096, 8192),
+        "nvgemm": (lambda r: orc.nv_gemm(*q["A4"], *q["B4"], rows=r), 8192, 8192, 8192),
+        "dsgemm": (lambda r: orc.ds_gemm(q["A5"][0], q["A5"][1], q["B5"][0], q["B5"][1], rows=r), 4096, 2048, 7168),
+    }
+    res = {}
+    for name in which:
+        fn, M, N, K = prods[name]
+        rows = np.linspace(0, M - 1, rows_per_gemm).astype(np.int64)
         t0 = time.perf_counter()
-        fn()
-        dt = time.perf_counter() - t0
-        t_total += dt * scale
-        parts.append(f"{what} x{scale:g}")
+        fn(rows)
+        res[name] = (time.perf_counter() - t0, 2.0 * len(rows) * N * K, 2.0 * M * N * K)
+    return res
 
-    x2 = synthetic.mxfp8_quantize(rows=256, cols=4096)
-    timed(lambda: [(orc.mx_quantize_rowwise(x2, f), orc.mx_quantize_colwise(x2, f)) for f in (0, 1)], 16384 / 256,
-          "q2 256 rows")
-    X, W, G = synthetic.mxfp8_linear(M=256, K=4096, N=256)
-    Gw = synthetic.normal(256, 14336, 1e-3, 3002)
-    def linq():
-        for src, f in ((X, 0), (W, 0)):
-            orc.mx_quantize_rowwise(src, f)
-            orc.mx_quantize_colwise(src, f)
-    timed(linq, (8192 + 14336) / 512, "X,W quantize 256 rows")
-    timed(lambda: (orc.mx_quantize_rowwise(Gw, 1), orc.mx_quantize_colwise(Gw, 1)), 8192 / 256, "G quantize 256 rows")
-    # GEMMs: a few output rows of each at full N and K
-    rng = np.random.default_rng(0)
-    def gemm_rows(M, N, K, fa, fb, rows):
-        qa = rng.integers(0, 0x7E, (rows, K), dtype=np.uint8)
-        qb = rng.integers(0, 0x7E, (N, K), dtype=np.uint8)
-        sa = np.full((rows, K // 32), 127, np.uint8)
-        sb = np.full((N, K // 32), 127, np.uint8)
-        timed(lambda: orc.mx_gemm(qa, sa, fa, qb, sb, fb), M / rows, f"mx gemm {rows} rows of {M}x{N}x{K}")
-    gemm_rows(8192, 14336, 4096, 0, 0, 4)
-    gemm_rows(8192, 4096, 14336, 1, 0, 4)
-    gemm_rows(14336, 4096, 8192, 1, 0, 4)
-    a4 = synthetic.with_sparse_outliers(128, 8192, 4000)
-    timed(lambda: orc.nv_quantize(a4), 2 * 8192 / 128, "nvfp4 quantize 128 rows")
-    qa4 = rng.integers(0, 256, (2, 4096), dtype=np.uint8)
-    qb4 = rng.integers(0, 256, (8192, 4096), dtype=np.uint8)
-    s4a = np.full((2, 512), 0x38, np.uint8)
-    s4b = np.full((8192, 512), 0x38, np.uint8)
-    timed(lambda: orc.nv_gemm(qa4, s4a, 1.0, qb4, s4b, 1.0), 8192 / 2, "nvfp4 gemm 2 rows of 8192^3")
-    a5 = synthetic.normal(256, 7168, 1.0, 5000)
-    timed(lambda: orc.ds_quantize_1x128(a5), 4096 / 256, "ds 1x128 quantize 256 rows")
-    b5 = synthetic.normal(256, 7168, 0.02, 5001)
-    timed(lambda: orc.ds_quantize_128x128(b5), 2048 / 256, "ds 128x128 quantize 256 rows")
-    qa5 = rng.integers(0, 0x7E, (4, 7168), dtype=np.uint8)
-    qb5 = rng.integers(0, 0x7E, (2048, 7168), dtype=np.uint8)
-    timed(lambda: orc.ds_gemm(qa5, np.ones((4, 56), np.float32), qb5, np.ones((16, 56), np.float32)), 4096 / 4,
-          "ds gemm 4 rows of 4096x2048x7168")
-    return t_total, "; ".join(parts), orc.num_threads()
+
+def oracle_step(host, quant_runs, rows_per_gemm, which=ORACLE_GEMMS):
+    """The CPU oracle on one bounded sample of the step: every quantizer on its full tensor
+    (the median of `quant_runs` runs), the products `which` on `rows_per_gemm` output rows each.
+    `value` is the GEMM FLOPs the sample computed over the seconds it took (quantizers included),
+    the metric the GPU step reports; the linear projection of the products to all their rows is
+    reported beside it (only when every product was sampled)."""
+    import oracle as orc
+    runs = []
+    q = None
+    for _ in range(quant_runs):
+        q, t = oracle_quantize_all(host)
+        runs.append(t)
+    tq = {k: statistics.median(r[k] for r in runs) for k in runs[0]}
+    g = oracle_gemm_sample(q, rows_per_gemm, which)
+    t_q = sum(tq.values())
+    t_g = sum(v[0] for v in g.values())
+    f_g = sum(v[1] for v in g.values())
+    t_proj = t_q + sum(v[0] * v[2] / v[1] for v in g.values())
+    return {
+        "value": f_g / (t_q + t_g) / 1e12, "unit": "TFLOP/s", "cores": orc.num_threads(), "kind": "oracle",
+        "seconds": t_q + t_g,
+        "sample": (f"every quantizer on its full tensor (median of {quant_runs}); {', '.join(which)} "
+                   f"on {rows_per_gemm} evenly spaced output rows each (all columns, full K); "
+                   "value = the sample's GEMM FLOPs / its seconds"),
+        "quantize_GB/s": round(sum(ORACLE_QUANT_BYTES.values()) / t_q / 1e9, 3),
+        "quantize_s": {k: round(v, 3) for k, v in tq.items()},
+        "gemm_GFLOP/s": round(f_g / t_g / 1e9, 3),
+        "projected_full_step_s": round(t_proj, 1) if len(which) == len(ORACLE_GEMMS) else None,
+        "projected_full_step_TFLOP/s": GEMM_FLOPS_STEP / t_proj / 1e12 if len(which) == len(ORACLE_GEMMS) else None,
+    }
 
 
 # ------------------------------------------------------------------------------------ main
@@ -552,6 +687,81 @@ def run_library_reference(args):
     return 0
 
 
+def headline(rows, rows_ms, present, peaks):
+    """The metric's two figures as top-level keys -- the MXFP8 linear-layer GEMMs' TFLOP/s and the
+    quantizers' GB/s -- and which rows meet the targets (quantizers >= 0.80 of HBM, block-scaled
+    GEMMs >= 0.70 of the dense peak), each against the derived and the nominal peak."""
+    out = {}
+    tpk = tensor_peaks(peaks)
+    lin = [n for n in ("fprop", "dgrad", "wgrad") if n in present]
+    if lin:
+        tf = len(lin) * F_LIN / (sum(rows_ms[n] for n in lin) / 1e3) / 1e12
+        out["mxfp8_gemm_tflops"] = round(tf, 1)
+        out["mxfp8_gemm_frac"] = round(tf / tpk["fp8"], 4)
+        out["mxfp8_gemm_frac_nominal"] = round(tf / NOMINAL_TFLOPS["fp8"], 4)
+    qrows = [n for n in present if "bytes" in rows[n]]
+    if qrows:
+        gbs = sum(rows[n]["bytes"] for n in qrows) / (sum(rows_ms[n] for n in qrows) / 1e3) / 1e9
+        out["quantize_gbs"] = round(gbs, 1)
+        out["quantize_frac"] = round(gbs / peaks["hbm_gbs"], 4)
+    tq = {n: rows[n]["frac"] for n in qrows}
+    tg = {n: (rows[n]["frac"], rows[n]["frac_nominal"]) for n in present if rows[n].get("bound") == "tensor"}
+    out["targets"] = {
+        "quantizers_hbm_0.80": {"met": sorted(n for n, f in tq.items() if f >= 0.80),
+                                "missed": {n: f for n, f in tq.items() if f < 0.80}},
+        "gemms_peak_0.70": {"met": sorted(n for n, (f, fn) in tg.items() if f >= 0.70),
+                            "missed": {n: f for n, (f, fn) in tg.items() if f < 0.70},
+                            "met_nominal": sorted(n for n, (f, fn) in tg.items() if fn >= 0.70),
+                            "missed_nominal": {n: fn for n, (f, fn) in tg.items() if fn < 0.70}},
+    }
+    return out
+
+
+def measure_mx512(dev, peaks, reps=200):
+    """MXFP8 512x512x512 (E4M3, FP32 out) from its seeded bf16 operands: the quantization of both
+    operands and the product, each timed per call with CUDA events on the launching stream
+    (median of `reps`).  A latency-bound case: its operands stay in L2 between calls."""
+    import torch
+    import block_scaled_precision_mx_gb300 as mx
+    from block_scaled_precision_mx_gb300 import synthetic
+    a, b = (t.to(dev) for t in synthetic.mxfp8_gemm_512())
+    sb = mx.mx_scale_bytes(512, 512)
+    qa, sa, qb, sb_ = (torch.empty(n, dtype=torch.uint8, device=dev) for n in (512 * 512, sb, 512 * 512, sb))
+    y = torch.empty(512, 512, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def quant():
+        mx.mx_quantize(a, layout=mx.ROWWISE, q_row=qa, s_row=sa)
+        mx.mx_quantize(b, layout=mx.ROWWISE, q_row=qb, s_row=sb_)
+
+    def gemm():
+        mx.mx_gemm(qa, sa, mx.E4M3, qb, sb_, mx.E4M3, 512, 512, 512, mx.OUT_F32, out=y)
+
+    def median_us(fn):
+        for _ in range(10):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(e0.elapsed_time(e1) for e0, e1 in ts) * 1e3
+
+    tq, tg = median_us(quant), median_us(gemm)
+    flops = 2 * 512 ** 3
+    tf = flops / (tg / 1e6) / 1e12
+    qbytes = 2 * mx_q_bytes(512, 512, copies=1)
+    return {"mx512": {"config": "MXFP8 E4M3 GEMM 512x512x512, FP32 out, operands quantized row-wise (E8M0 per 32)",
+                      "gemm_us": round(tg, 2), "TFLOP/s": round(tf, 1),
+                      "frac": round(tf / tensor_peaks(peaks)["fp8"], 5),
+                      "frac_nominal": round(tf / NOMINAL_TFLOPS["fp8"], 5),
+                      "quantize_us": round(tq, 2), "quantize_GB/s": round(qbytes / (tq / 1e6) / 1e9, 1),
+                      "reps": reps, "bound": "latency (2 launches / 1 launch of a few microseconds; L2-resident)"}}
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -559,24 +769,48 @@ def dist_env():
     return rank, world, local
 
 
+BASE_CONFIG = {"workload": WORKLOAD,
+               "l2": "inputs larger than L2 (129 MB) between reuses; no explicit flush",
+               "rows": "per-row times and roofline from a second timed pass of the same K steps with an "
+                       "event at every row boundary; value from K steps with none"}
+
+
 def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample of the step per
+    timed step (rank 0 only; other ranks exit without work)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    t_steps = []
-    desc = threads = None
+    import oracle as orc
+    orc.build()
+    host = make_host_inputs(Workload.GROUPS)
+    # each step: every quantizer on its full tensor and one product (in turn) on one output row
+    # per host thread, so that K + W steps take a few minutes
+    rows = orc.num_threads()
+    samples = []
+    t0 = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        t, desc, threads = oracle_sample_run()
+        r = oracle_step(host, 1, rows, (ORACLE_GEMMS[i % len(ORACLE_GEMMS)],))
         if i >= args.warmup:
-            t_steps.append(t)
-    t_step = statistics.median(t_steps)
-    value = GEMM_FLOPS_STEP / t_step / 1e12
+            samples.append(r)
+    wall = time.perf_counter() - t0
+    sec = sum(r["seconds"] for r in samples)
+    flops = sum(r["value"] * 1e12 * r["seconds"] for r in samples)
+    value = flops / sec / 1e12
+    cpu = dict(samples[-1])
+    cpu["value"] = value
+    cpu["sample"] = ("per step: every quantizer on its full tensor; one of " + ", ".join(ORACLE_GEMMS) +
+                     f" in turn on {rows} evenly spaced output rows (all columns, full K); value = the steps' "
+                     "GEMM FLOPs / their seconds")
+    for k in ("seconds", "projected_full_step_s", "projected_full_step_TFLOP/s", "quantize_s", "gemm_GFLOP/s"):
+        cpu.pop(k, None)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "sample": "bounded sample of each row, projected to the full step"},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "warmup": args.warmup, "ms_per_step": sec / len(samples) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": dict(BASE_CONFIG, parallelism=f"replicas x{world}"),
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
     print(json.dumps(line))
     return 0
 
@@ -602,10 +836,14 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     rank, world, local = dist_env()
-    # the oracle's OpenMP pool is created before the first GPU call
+    groups = tuple(args.only.split(",")) if args.only else Workload.GROUPS
+    host = make_host_inputs(groups)
+    # the oracle runs (and its OpenMP pool is created) before the first GPU call
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_sample_run()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
+        import oracle as orc
+        orc.build()
+        cpu = oracle_step(host, 3, orc.num_threads())
 
     import torch
     import block_scaled_precision_mx_gb300 as mx
@@ -620,8 +858,7 @@ def main():
         pg = dist
     peaks = load_peaks()
 
-    groups = tuple(args.only.split(",")) if args.only else Workload.GROUPS
-    wl = Workload(dev, groups)
+    wl = Workload(dev, groups, host=host)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         wl.step()
@@ -637,10 +874,7 @@ def main():
             lst.append((name, e))
         return mark
 
-    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if os.environ.get(
-        "CUDA_VISIBLE_DEVICES") else str(local)
-    sampler = ClockSampler(phys)
-    sampler.start()
+    sampler = clock_sampler(local)
     time.sleep(0.3)
     if pg:
         pg.barrier()
@@ -680,10 +914,8 @@ def main():
     rows_ms = {n: v / len(evs) for n, v in rows_ms.items()}
     present = [n for n in ROW_ORDER if rows_ms[n] > 0]
     rows = {n: row_report(n, rows_ms[n], peaks) for n in present}
-    row_flops = {"fprop": F_LIN, "dgrad": F_LIN, "wgrad": F_LIN, "nvgemm": F_NV, "dsgemm": F_DS, "mx4gemm": F_MX4,
-                 "blkgemm": F_DS, "moegemm": F_MOE, "moe4gemm": F_MOE, "moedsgemm": F_MOE, "fusedgemm": F_LIN,
-                 "fusedboth": F_LIN}
-    step_flops = sum(row_flops.get(n, 0) for n in present)
+    # the unfused comparison repeats the fused rows' product: its FLOPs are not counted again
+    step_flops = sum(ROW_FLOPS.get(n, 0) for n in present if n != "unfused")
 
     # dominant kernel: the kernel (all its launches in the step) with the largest share
     kernels = {"mx_gemm": ["fprop", "dgrad", "wgrad"], "nvfp4_gemm": ["nvgemm"], "fp8_blockwise_gemm": ["dsgemm"],
@@ -711,21 +943,23 @@ def main():
     if os.path.exists(tpath):
         with open(tpath) as f:
             traffic = json.load(f).get(dom)
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    tpk = tensor_peaks(peaks)
     gemm_flops = {"mx_gemm": len(kernels.get("mx_gemm", [])) * F_LIN, "nvfp4_gemm": F_NV, "fp8_blockwise_gemm": F_DS,
                   "mxfp4_gemm": F_MX4, "mx_gemm_blocks": F_DS, "mx_gemm_grouped": F_MOE, "nvfp4_gemm_grouped": F_MOE,
                   "fp8_blockwise_gemm_grouped": F_MOE, "mx_gemm_mxout": len(kernels.get("mx_gemm_mxout", [])) * F_LIN,
                   "mx_gemm_then_quantize": F_LIN}
     if dom in gemm_flops:
         flops = gemm_flops[dom]
-        fp4 = dom in ("nvfp4_gemm", "mxfp4_gemm", "nvfp4_gemm_grouped")
-        peak = 3 * fp8_peak if fp4 else fp8_peak
+        kind = "fp4" if dom in ("nvfp4_gemm", "mxfp4_gemm", "nvfp4_gemm_grouped") else "fp8"
+        peak = tpk[kind]
         ach = flops / (dom_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": dom, "achieved": round(ach, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": traffic,
+                "frac_nominal": round(ach / NOMINAL_TFLOPS[kind], 4), "peak_nominal": NOMINAL_TFLOPS[kind],
                 "per_launch": {"flops": flops // launches[dom], "avg_ms": round(dom_ms / launches[dom], 4)},
-                "peak_source": f"{peaks['source']}: bf16 sustained x {'6 (FP4)' if fp4 else '2 (FP8)'}"
-                               " nominal dense ratio"}
+                "peak_source": f"derived ({kind.upper()}): " + tpk["source"]}
+        if ach > peak:
+            roof["note"] = "achieved above the derived peak: the peak understates this GPU's rate at the clock seen"
     else:
         b = sum(rows[r]["bytes"] for r in kernels[dom])
         ach = b / (dom_ms / 1e3) / 1e9
@@ -734,6 +968,9 @@ def main():
                 "per_launch": {"bytes": int(b // launches[dom]), "avg_ms": round(dom_ms / launches[dom], 4)},
                 "peak_source": f"{peaks['source']} copy bandwidth"}
     roof["launches_per_step"] = launches[dom]
+
+    # configuration of the 512^3 product: timed on its own (a latency-bound case, not in the step)
+    latency = measure_mx512(dev, peaks) if not args.only else None
 
     # end to end through the public API with host buffers
     e2e = None
@@ -797,24 +1034,16 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8/fp4 inputs, f32 accumulate", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (129 MB) between reuses; no explicit flush",
-                   "rows": "per-row times and roofline from a second timed pass of the same K steps with an "
-                           "event at every row boundary; value from K steps with none",
-                   "quantize_GB/s": round(sum(rows[n]["bytes"] for n in present if "bytes" in rows[n]) /
-                                          (sum(rows_ms[n] for n in present if "bytes" in rows[n]) / 1e3) / 1e9, 1)
-                   if any("bytes" in rows[n] for n in present) else None},
-        "rows": rows,
-        "roofline": roof,
-        "gpu_launches": wl.launches_per_step * args.steps,
-        "clocks": clocks,
-        "e2e": e2e,
+        "config": dict(BASE_CONFIG, parallelism=f"replicas x{world}"),
     }
+    line.update(headline(rows, rows_ms, present, peaks))
+    line.update({"rows": rows, "roofline": roof, "gpu_launches": wl.launches_per_step * args.steps,
+                 "clocks": clocks, "e2e": e2e})
+    if latency is not None:
+        line["latency"] = latency
     if cpu is not None:
-        t_cpu, desc, threads = cpu
-        line["cpu_baseline"] = {"value": round(GEMM_FLOPS_STEP / t_cpu / 1e12, 6), "unit": "TFLOP/s",
-                                "cores": threads, "kind": "oracle", "sample": desc,
-                                "projected_step_s": round(t_cpu, 2)}
+        cpu.pop("seconds", None)
+        line["cpu_baseline"] = cpu
     if args.only:
         line["config"]["only"] = args.only
         line["note"] = "profiling subset (--only): not a bench value"

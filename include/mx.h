@@ -378,9 +378,12 @@ mx_status fp8_blockwise_gemm(const void* qa, const float* sa,
  * Arguments and results are those of nvfp4_quantize (identical codes, scales and gscale).
  * Limit: rows <= 262144 (the array holds one partial maximum per 16 rows); larger inputs return
  * MX_ERR_INVALID_ARG.  The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.  All calls share the one
- * array: calls that overlap on the GPU (different streams, or different host threads, without
- * ordering between them) race and may produce wrong results.  Each call writes every scratch slot
+ * that device current); make that first call before any stream capture.  The address is cached
+ * per device ordinal, so the library assumes that every call on a device runs in the CUDA
+ * runtime's primary context of that device (the context the runtime API and PyTorch use); a
+ * caller that makes its own driver-API contexts must not call this entry point from them.  All
+ * calls share the one array: calls that overlap on the GPU (different streams, or different host
+ * threads, without ordering between them) race and may produce wrong results.  Each call writes every scratch slot
  * it reads before reading it, so nothing left by an earlier call needs clearing.
  */
 mx_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols,

@@ -4,9 +4,10 @@ Bar (per output element, on the decoded operands): |y - y_ref| <= 1e-5 * sum_k |
 FP32 output; bf16 output adds one bf16 ulp of |y_ref| for the final rounding.  Cases: the
 512^3 MXFP8 workload in full, tiny-K brute force with codes over the whole finite range,
 one-hot scale probes (confirm the scale layout the tensor core reads by behaviour), mixed
-E5M2 x E4M3, the 8192x4096x14336 fprop / dgrad / wgrad trio on sampled rows, NVFP4 (the
-scale-outside-the-sum identity, 8192^3 on sampled rows) and the DeepSeek GEMM with promotion
-(4096x7168x2048 on sampled rows; error independent of K).
+E5M2 x E4M3, the 8192x4096x14336 fprop / dgrad / wgrad trio, NVFP4 (the scale-outside-the-sum
+identity, 8192^3) and the DeepSeek GEMM with promotion (4096x7168x2048; error independent of K) at
+full size on one row of every 128-row tile (all columns), and a 4096x2560 output (more tiles than
+CTA pairs) in full for all three products.
 """
 import numpy as np
 import pytest
@@ -48,6 +49,14 @@ def assert_close(got, ref, absum, bf16=False, what=""):
 
 def to_dev_u8(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def tile_rows(M, salt=0):
+    """One output row from every 128-row M tile (all N columns are checked): row
+    t * 128 + (37 t + 5 + salt) % 128 of tile t.  Consecutive tiles take rows of different TMEM lane
+    quarters, and each 256-row CTA-pair tile has one row in each of its two CTAs, so every tile the
+    persistent scheduler hands out -- first or later tile of a CTA -- is compared somewhere."""
+    return np.array([t * 128 + (37 * t + 5 + salt) % 128 for t in range(M // 128)], dtype=np.int64)
 
 
 # ------------------------------------------------------------------ MXFP8
@@ -177,9 +186,6 @@ def linear_layer():
     return quantized.mx_both(x, orc.E4M3), quantized.mx_both(w, orc.E4M3), quantized.mx_both(g, orc.E5M2)
 
 
-SAMPLE_ROWS = [0, 1, 127, 128, 4095, 5000, 8191]
-
-
 @pytest.mark.parametrize("which", ["fprop", "dgrad", "wgrad"])
 def test_mx_linear_layer_full_size(linear_layer, which):
     (Xd, Xo), (Wd, Wo), (Gd, Go) = linear_layer
@@ -195,10 +201,55 @@ def test_mx_linear_layer_full_size(linear_layer, which):
         (A, Ao), (B, Bo) = (Gd, Go), (Xd, Xo)
     y = mx.mx_gemm(A[a[0]], A[a[1]], ea, B[b[0]], B[b[1]], eb, M, N, K, out_dtype=mx.OUT_BF16)
     assert mx.mx_check() == mx.MX_OK
-    rows = np.array(sorted(set(r % M for r in SAMPLE_ROWS + [M - 1, M // 2 + 3])))
+    rows = tile_rows(M)
     ref, ab = orc.mx_gemm(Ao[a[0]], Ao[a[1]], ea, Bo[b[0]], Bo[b[1]], eb, rows=rows)
     got = y[torch.from_numpy(rows).cuda()].float().cpu().numpy()
     assert_close(got, ref, ab, bf16=True, what=which)
+
+
+# ------------------------------------------------------------------ more tiles than CTA pairs, in full
+# 4096 x 2560: 160 pair tiles of 256 x 256 for the persistent grid of CTA pairs (76 on 152 SMs),
+# so most CTAs take a second or third tile and the accumulator / stage phases wrap across tiles;
+# every output element is compared with the oracle.
+MID = (4096, 2560)
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_mx_gemm_more_tiles_than_pairs_in_full(out_dtype):
+    M, N = MID
+    K = 256
+    a = synthetic.normal(M, K, 1.0, 8100)
+    b = synthetic.normal(N, K, 0.02, 8101)
+    qa, sa, oqa, osa = quantized.mx_rowwise(a, orc.E4M3)
+    qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E4M3)
+    y = mx.mx_gemm(qa, sa, mx.E4M3, qb, sb, mx.E4M3, M, N, K, out_dtype=out_dtype)
+    assert mx.mx_check() == mx.MX_OK
+    ref, ab = orc.mx_gemm(oqa, osa, orc.E4M3, oqb, osb, orc.E4M3)
+    assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="mx 4096x2560x256")
+
+
+def test_nvfp4_gemm_more_tiles_than_pairs_in_full():
+    M, N = MID
+    K = 256
+    a = synthetic.with_sparse_outliers(M, K, 8200)
+    b = synthetic.with_sparse_outliers(N, K, 8201)
+    qa, sa, ga, oqa, osa, oga = quantized.nv(a)
+    qb, sb, gb, oqb, osb, ogb = quantized.nv(b)
+    y = mx.nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=mx.OUT_F32)
+    assert mx.mx_check() == mx.MX_OK
+    ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb)
+    assert_close(y.cpu().numpy(), ref, ab, what="nvfp4 4096x2560x256")
+
+
+@pytest.mark.parametrize("out_dtype", [mx.OUT_F32, mx.OUT_BF16])
+def test_deepseek_gemm_more_tiles_than_pairs_in_full(out_dtype):
+    M, N = MID
+    K = 256
+    a = synthetic.normal(M, K, 1.0, 8300)
+    b = synthetic.normal(N, K, 0.02, 8301)
+    y, qa, sa, qb, sb = ds_run(a, b, out_dtype=out_dtype)
+    ref, ab = orc.ds_gemm(qa, sa, qb, sb)
+    assert_close(y.float().cpu().numpy(), ref, ab, bf16=out_dtype == mx.OUT_BF16, what="deepseek 4096x2560x256")
 
 
 # ------------------------------------------------------------------ NVFP4
@@ -249,7 +300,7 @@ def test_nvfp4_gemm_full_size():
     M = N = K = 8192
     y = mx.nvfp4_gemm(qa, sa, ga, qb, sb, gb, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    rows = np.array([0, 1, 129, 4096, 8191])
+    rows = tile_rows(M)
     ref, ab = orc.nv_gemm(oqa, osa, oga, oqb, osb, ogb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="nvfp4 8192^3")
 
@@ -320,7 +371,7 @@ def test_deepseek_gemm_full_size():
     M, K = a.shape
     N = b.shape[0]
     y, qa, sa, qb, sb = ds_run(a, b, out_dtype=mx.OUT_BF16)
-    rows = np.array([0, 5, 128, 2049, 4095])
+    rows = tile_rows(M)
     ref, ab = orc.ds_gemm(qa, sa, qb, sb, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].float().cpu().numpy(), ref, ab, bf16=True, what="deepseek full")
 

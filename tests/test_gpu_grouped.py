@@ -17,7 +17,7 @@ import torch
 import block_scaled_precision_mx_gb300 as mx
 import oracle as orc
 from tests.layouts import chunked_to_plain, pack_fp4, plain_to_chunked
-from tests.test_gpu_gemm import assert_close
+from tests.test_gpu_gemm import assert_close, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,8 @@ def run_grouped(sizes, N, K, out_dtype, seed, sample=None):
         lo, hi = int(off[g]), int(off[g + 1])
         if hi == lo:
             continue
-        rows = np.arange(hi - lo) if sample is None else np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64))
+        rows = (np.arange(hi - lo) if sample is None else tile_rows(hi - lo, salt=g) if sample == "tiles" else
+                np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64)))
         ref, ab = orc.mx_gemm(qa[lo:hi], sa[lo:hi], orc.E4M3, qb[g * N:(g + 1) * N], sb[g * N:(g + 1) * N], orc.E4M3,
                               rows=rows)
         assert_close(yn[lo + rows], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"group {g}")
@@ -70,7 +71,13 @@ def test_grouped_half_tiles_and_empty_groups(out_dtype):
 def test_grouped_many_groups_moe_shape():
     rng = np.random.default_rng(2)
     sizes = (rng.integers(0, 9, 16) * 128).tolist()           # 16 experts, 0 .. 1024 rows each
-    run_grouped(sizes, 1024, 2048, mx.OUT_BF16, seed=3, sample=24)
+    run_grouped(sizes, 1024, 2048, mx.OUT_BF16, seed=3, sample="tiles")
+
+
+def test_grouped_moe_workload_shape_every_tile():
+    # the bench's grouped MXFP8 workload: 8 experts 4096 -> 14336, 16384 routed rows split unevenly;
+    # one row of every 128-row tile of every expert, all columns
+    run_grouped([3328, 1536, 2432, 1024, 2816, 1920, 2176, 1152], 14336, 4096, mx.OUT_BF16, seed=5, sample="tiles")
 
 
 def test_single_group_equals_plain_gemm():
@@ -295,7 +302,8 @@ def run_ds_grouped(sizes, N, K, out_dtype, seed, sample=None):
         lo, hi = int(off[g]), int(off[g + 1])
         if hi == lo:
             continue
-        rows = np.arange(hi - lo) if sample is None else np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64))
+        rows = (np.arange(hi - lo) if sample is None else tile_rows(hi - lo, salt=g) if sample == "tiles" else
+                np.unique(np.linspace(0, hi - lo - 1, sample).astype(np.int64)))
         ref, ab = orc.ds_gemm(qa[lo:hi], sa[lo:hi], qb[g * N:(g + 1) * N], sb[g * N // 128:(g + 1) * N // 128], rows=rows)
         assert_close(yn[lo + rows], ref, ab, bf16=out_dtype == mx.OUT_BF16, what=f"deepseek group {g}")
     return qa, sa, qb, sb, off, y
@@ -306,9 +314,10 @@ def test_ds_grouped_half_tiles_and_empty_groups(out_dtype):
     run_ds_grouped([128, 384, 0, 256, 128], 256, 512, out_dtype, 9900)
 
 
-def test_ds_grouped_moe_shape_sampled():
-    # the grouped-GEMM workload: 8 experts 4096 -> 14336, 16384 routed rows split unevenly
-    run_ds_grouped([3328, 1536, 2432, 1024, 2816, 1920, 2176, 1152], 14336, 4096, mx.OUT_BF16, 9910, sample=6)
+def test_ds_grouped_moe_shape_every_tile():
+    # the grouped-GEMM workload: 8 experts 4096 -> 14336, 16384 routed rows split unevenly; one row of
+    # every 128-row tile of every expert, all columns
+    run_ds_grouped([3328, 1536, 2432, 1024, 2816, 1920, 2176, 1152], 14336, 4096, mx.OUT_BF16, 9910, sample="tiles")
 
 
 def test_ds_grouped_single_group_equals_plain_gemm():

@@ -18,7 +18,7 @@ import oracle as orc
 from tests import quantized
 from tests.layouts import chunked_to_plain, pack_fp4, plain_to_chunked, unpack_fp4
 from tests.test_gpu_quantize import exhaustive_matrix
-from tests.test_gpu_gemm import assert_close
+from tests.test_gpu_gemm import assert_close, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -137,6 +137,6 @@ def test_mxfp4_quantize_then_gemm_full_size():
     qb, sb, oqb, osb = quantized.mx_rowwise(b, orc.E2M1)
     y = mx.mx_gemm(qa, sa, mx.E2M1, qb, sb, mx.E2M1, M, N, K, out_dtype=mx.OUT_F32)
     assert mx.mx_check() == mx.MX_OK
-    rows = np.array([0, 1, 255, 256, 4097, 8191])
+    rows = tile_rows(M)
     ref, ab = orc.mx_gemm(oqa, osa, orc.E2M1, oqb, osb, orc.E2M1, rows=rows)
     assert_close(y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, ab, what="mxfp4 8192^3")
