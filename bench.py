@@ -750,7 +750,32 @@ def measure_mx512(dev, peaks, reps=200):
         torch.cuda.synchronize()
         return statistics.median(e0.elapsed_time(e1) for e0, e1 in ts) * 1e3
 
+    def graph_us(fn, n=50):
+        """Device time per call from a CUDA graph of n back-to-back calls (no per-call host work)."""
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                fn()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(n):
+                        fn()
+            stream.wait_stream(side)
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / n
+        except Exception:  # noqa: BLE001 -- capture unsupported here: report the per-call time only
+            torch.cuda.synchronize()
+            return None
+
     tq, tg = median_us(quant), median_us(gemm)
+    gq, gg = graph_us(quant), graph_us(gemm)
     flops = 2 * 512 ** 3
     tf = flops / (tg / 1e6) / 1e12
     qbytes = 2 * mx_q_bytes(512, 512, copies=1)
@@ -759,7 +784,12 @@ def measure_mx512(dev, peaks, reps=200):
                       "frac": round(tf / tensor_peaks(peaks)["fp8"], 5),
                       "frac_nominal": round(tf / NOMINAL_TFLOPS["fp8"], 5),
                       "quantize_us": round(tq, 2), "quantize_GB/s": round(qbytes / (tq / 1e6) / 1e9, 1),
-                      "reps": reps, "bound": "latency (2 launches / 1 launch of a few microseconds; L2-resident)"}}
+                      "gemm_us_graph": None if gg is None else round(gg, 2),
+                      "quantize_us_graph": None if gq is None else round(gq, 2),
+                      "reps": reps,
+                      "timing": "*_us: CUDA events around each call (host-side tensor-map encoding and launch "
+                                "included); *_us_graph: per call inside a CUDA graph of 50 back-to-back calls",
+                      "bound": "latency (2 launches / 1 launch of a few microseconds; L2-resident)"}}
 
 
 def dist_env():
