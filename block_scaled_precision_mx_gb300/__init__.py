@@ -56,6 +56,8 @@ def library_path() -> str:
 def load():
     """Load libmxgb.so (built by build.py / __graft_entry__.build()).  Raises if missing."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -122,8 +124,13 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:   # the current stream's handle without building a Stream object
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -165,12 +172,11 @@ def mx_quantize(x: torch.Tensor, block: int = 32, block_rows: int = 1, elem: int
             shape = (cols // 128, rows) if block_rows == 1 else (rows // 128, cols // 128)
             s_row = torch.empty(shape, dtype=torch.float32, device=dev)
     else:
-        nb = mx_scale_bytes(rows, cols, block, block_rows, sfmt)
         per_byte = 2 if elem == E2M1 else 1          # MXFP4 codes are packed two per byte
         if row and q_row is None:
             q_row = torch.empty(rows, cols // per_byte, dtype=torch.uint8, device=dev)
         if row and s_row is None:
-            s_row = _u8(nb, dev)
+            s_row = _u8(mx_scale_bytes(rows, cols, block, block_rows, sfmt), dev)
         if col and q_col is None:
             q_col = torch.empty(cols, rows // per_byte, dtype=torch.uint8, device=dev)
         if col and s_col is None:

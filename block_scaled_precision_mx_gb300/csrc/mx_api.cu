@@ -69,20 +69,69 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
+// 2-D tensor maps, remembered: a map depends only on the arguments of its encoding (address,
+// shape, stride, box, element type, swizzle, L2 promotion), so repeated calls on the same buffers
+// (a training step, a benchmark loop) copy a stored map instead of encoding it again.  A small
+// direct-mapped table under a mutex; a slot holds the last map whose key hashed there.
+struct TmapKey {
+  const void* base;
+  uint64_t dim0, dim1, stride;
+  uint32_t box0, box1;
+  int dtype, swizzle, promo;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && dim0 == o.dim0 && dim1 == o.dim1 && stride == o.stride && box0 == o.box0 &&
+           box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle && promo == o.promo;
+  }
+};
+struct TmapSlot {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kTmapSlots = 256;
+TmapSlot g_tmaps[kTmapSlots];
+std::mutex g_tmap_mu;
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0, uint64_t dim1,
+               uint64_t stride, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle,
+               CUtensorMapL2promotion promo) {
+  const TmapKey key{base, dim0, dim1, stride, box0, box1, static_cast<int>(dtype), static_cast<int>(swizzle),
+                    static_cast<int>(promo)};
+  uint64_t h = reinterpret_cast<uintptr_t>(base) >> 8;
+  h ^= dim0 * 0x9E3779B97F4A7C15ull ^ dim1 * 0xC2B2AE3D27D4EB4Full ^ (static_cast<uint64_t>(box1) << 20) ^
+       static_cast<uint64_t>(swizzle) * 131 ^ static_cast<uint64_t>(dtype) * 977;
+  TmapSlot& slot = g_tmaps[(h ^ (h >> 29)) % kTmapSlots];
+  {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    if (slot.valid && slot.key == key) {
+      *map = slot.map;
+      return true;
+    }
+  }
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {dim0, dim1};
+  cuuint64_t strides[1] = {stride};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t estr[2] = {1u, 1u};
+  if (fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+         promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  slot.key = key;
+  slot.map = *map;
+  slot.valid = true;
+  return true;
+}
+
 // 2-D byte tensor [rows][row_bytes], box 128 bytes x box_rows, 128-byte swizzle (swizzle=false:
 // unswizzled, used for scale chunks read as 128-byte rows).
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, int box_rows,
                bool swizzle = true) {
-  auto fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, static_cast<uint64_t>(row_bytes),
+                   static_cast<uint64_t>(rows), static_cast<uint64_t>(row_bytes), 128u,
+                   static_cast<uint32_t>(box_rows), swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // ---------------------------------------------------------------- device properties
@@ -133,16 +182,10 @@ mx_status launch_gemm(const void* qa, const void* qb, int64_t kbytes, const Gemm
 // Output tensor map: [M][ldc] elements, 32 x 32 boxes, swizzle matching the epilogues' staging
 // layout (64-byte rows for bf16, 128-byte rows for FP32).
 bool make_out_tmap(CUtensorMap* map, void* out, int64_t M, int64_t N, int64_t ldc, bool bf16) {
-  auto fn = get_encode_fn();
-  if (!fn) return false;
-  const size_t es = bf16 ? 2 : 4;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc * es)};
-  cuuint32_t box[2] = {32u, 32u};
-  cuuint32_t estr[2] = {1u, 1u};
-  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t es = bf16 ? 2 : 4;
+  return encode_2d(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out,
+                   static_cast<uint64_t>(N), static_cast<uint64_t>(M), static_cast<uint64_t>(ldc) * es, 32u, 32u,
+                   bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 // Launch a CTA-pair kernel: clusters of two CTAs, as many clusters as fit on the device at once
