@@ -91,6 +91,34 @@ def test_mx_gemm_tiny_bruteforce(M, K, fa, fb):
     assert_close(y, ref, ab, what="tiny")
 
 
+def test_mx_gemm_same_addresses_other_shapes():
+    # The library remembers encoded TMA tensor maps keyed by every encoding argument.  The same
+    # device buffers are used here with other row counts, other K (so other row strides) and
+    # other contents in turn; every call must match the oracle, as it would if each call encoded
+    # its maps afresh.
+    rng = np.random.default_rng(4242)
+    qa_buf = torch.empty(512 * 512, dtype=torch.uint8, device="cuda")
+    qb_buf = torch.empty(512 * 512, dtype=torch.uint8, device="cuda")
+    sa_buf = torch.empty(mx.mx_scale_bytes(512, 512), dtype=torch.uint8, device="cuda")
+    sb_buf = torch.empty(mx.mx_scale_bytes(512, 512), dtype=torch.uint8, device="cuda")
+    y_buf = torch.empty(512 * 512, dtype=torch.float32, device="cuda")
+    for (M, N, K) in [(256, 256, 256), (512, 256, 256), (256, 512, 512), (256, 256, 256), (512, 512, 128),
+                      (128, 256, 512)]:
+        qa, qb = random_codes(rng, (M, K), orc.E4M3), random_codes(rng, (N, K), orc.E4M3)
+        sa = rng.integers(115, 140, (M, K // 32), dtype=np.uint8)
+        sb = rng.integers(115, 140, (N, K // 32), dtype=np.uint8)
+        csa, csb = plain_to_chunked(sa), plain_to_chunked(sb)
+        qa_buf[: M * K].copy_(torch.from_numpy(qa.reshape(-1)))
+        qb_buf[: N * K].copy_(torch.from_numpy(qb.reshape(-1)))
+        sa_buf[: csa.size].copy_(torch.from_numpy(csa.reshape(-1)))
+        sb_buf[: csb.size].copy_(torch.from_numpy(csb.reshape(-1)))
+        y = mx.mx_gemm(qa_buf, sa_buf, mx.E4M3, qb_buf, sb_buf, mx.E4M3, M, N, K, out_dtype=mx.OUT_F32,
+                       out=y_buf[: M * N].view(M, N))
+        assert mx.mx_check() == mx.MX_OK
+        ref, ab = orc.mx_gemm(qa, sa, orc.E4M3, qb, sb, orc.E4M3)
+        assert_close(y.cpu().numpy(), ref, ab, what=f"{M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("N", [128, 256])       # 256 with M = 256: CTA-pair kernel
 def test_mx_gemm_one_hot_scale_probe(N):
     # all scales 2^0 except one (row r, k-block b) = 2^1: exactly the outputs of row r (or column
