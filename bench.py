@@ -787,8 +787,9 @@ def measure_mx512(dev, peaks, reps=200):
                       "gemm_us_graph": None if gg is None else round(gg, 2),
                       "quantize_us_graph": None if gq is None else round(gq, 2),
                       "reps": reps,
-                      "timing": "*_us: CUDA events around each call (host-side tensor-map encoding and launch "
-                                "included); *_us_graph: per call inside a CUDA graph of 50 back-to-back calls",
+                      "timing": "*_us: CUDA events around each call (the binding's argument marshalling, the "
+                                "library's tensor-map lookup and the launch included); *_us_graph: per call inside "
+                                "a CUDA graph of 50 back-to-back calls",
                       "bound": "latency (2 launches / 1 launch of a few microseconds; L2-resident)"}}
 
 
