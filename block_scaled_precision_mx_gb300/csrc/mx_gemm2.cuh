@@ -517,8 +517,9 @@ __global__ void __launch_bounds__(Gemm2Cfg<KIND, OUT_BF16 || (MXOUT >= 0), GROUP
         // (30 ns per k-step of the tile between chunks, about a quarter of the tile's time in
         // all) instead of in one burst from every SM at once; the bursts slowed the operand
         // loads.  Measured at 8192^3: NVFP4 195.6 -> 191.1 us, MXFP4 180.1 -> 176.7 us, MXFP8
-        // (K = 4096) 307.1 -> 302.9 us; bf16 output gained nothing and is not spaced.
-        if (!OUT_BF16 && c > 0) __nanosleep(static_cast<unsigned>(num_kt) * 30u);
+        // (K = 4096) 307.1 -> 302.9 us; bf16 output gained nothing and is not spaced, nor is a
+        // CTA's last tile (no main loop follows it).
+        if (!OUT_BF16 && c > 0 && tile + nclusters < num_tiles) __nanosleep(static_cast<unsigned>(num_kt) * 30u);
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
